@@ -1,0 +1,157 @@
+/*
+ * wq.h -- C ABI of libwq, weight-only quantized matrix multiply on GB300 (sm_103a).
+ *
+ *   y[m, n] = sum_k x[m, k] * w[k, n],   w[k, n] = (q[k, n] - zero[g, n]) * scale[g, n],
+ *   g = k / group_size,
+ *
+ * with q an unsigned w_bit-bit code (w_bit 2 or 4) packed 32/w_bit per int32
+ * along K, as stated by BitDistiller, quantization/triton_kernels.py,
+ * quant_matmul_kernel (docstring: "a: (M, K), qw: (K // pack_num, N),
+ * scales: (K // group_size, N), qzeros: (K // group_size // pack_num, N)";
+ * K loop: field = (packed >> ((k % pack_num) * w_bit)) & offset).  That page is
+ * cut off before the scale/zero step; this library takes (q - zero) * scale.
+ * Two special cases are covered:
+ *   - symmetric int4 with the zero fixed at 8 (zeros == NULL), as in the
+ *     dequant() of aphrodite-engine marlin_cuda_kernel.cu, which folds "-8"
+ *     into its subtraction; symmetric int2 takes zero 2;
+ *   - int8 weights with one fp32 scale per output channel, y[m, n] =
+ *     scale[n] * sum_k x[m, k] * q[n, k] (tiny-llm kernels/int8_gemv.py,
+ *     int8_matmul docstring: x (M, K) bf16/fp16, q (N, K) int8, scale (N,) fp32
+ *     -> y (M, N) fp32).
+ *
+ * Conventions shared by every entry point.
+ *   - Every array pointer is a DEVICE pointer owned by the caller.  The library
+ *     allocates nothing, never synchronises (except wq_check_device), and
+ *     enqueues its kernels on `stream` (a cudaStream_t passed as void*; NULL is
+ *     the legacy default stream).
+ *   - Arguments are validated on the host before anything is launched; an
+ *     invalid call returns a status and enqueues nothing.  No exception or
+ *     longjmp crosses this ABI.
+ *   - Layouts are row-major and dense (no strides).
+ *   - Launch failures are reported as WQ_ERR_CUDA.  A device-side wait that
+ *     gives up (bounded spin on a shared-memory barrier) records a flag that
+ *     wq_check_device() turns into WQ_ERR_TIMEOUT; the kernel then returns
+ *     without faulting.
+ *   - The library keeps no state besides a per-device cache of the SM count
+ *     and the kernels' shared-memory attributes.
+ */
+#ifndef WQ_H
+#define WQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define WQ_API __attribute__((visibility("default")))
+#else
+#define WQ_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    WQ_OK = 0,
+    WQ_ERR_NULL = 1,       /* a required pointer is NULL                               */
+    WQ_ERR_SHAPE = 2,      /* M, N, K negative, zero where not allowed, or not divisible */
+    WQ_ERR_WBIT = 3,       /* w_bit not in {2, 4, 8}                                   */
+    WQ_ERR_GROUP = 4,      /* group_size does not divide K or is not a multiple of 16  */
+    WQ_ERR_DTYPE = 5,      /* unsupported x or scale dtype for this w_bit              */
+    WQ_ERR_ALIGN = 6,      /* a pointer is not 16-byte aligned                         */
+    WQ_ERR_WORKSPACE = 7,  /* workspace NULL or smaller than wq_workspace_bytes()      */
+    WQ_ERR_ARCH = 8,       /* current device is not compute capability 10.3            */
+    WQ_ERR_CUDA = 9,       /* a CUDA runtime call or kernel launch failed              */
+    WQ_ERR_TIMEOUT = 10    /* a kernel gave up waiting on one of its own barriers      */
+} wq_status;
+
+typedef enum { WQ_F16 = 0, WQ_BF16 = 1, WQ_F32 = 2 } wq_dtype;
+
+/* Human-readable name of a status; never NULL. */
+WQ_API const char *wq_status_string(wq_status s);
+
+/*
+ * Number of values along K that one packed chunk row spans: 256 / w_bit
+ * (128 for w_bit 2, 64 for 4, 32 for 8).  K must be a multiple of it.
+ */
+WQ_API int wq_chunk_k(int w_bit);
+
+/*
+ * Bytes of the packed weight buffer that wq_pack writes: K * N * w_bit / 8,
+ * the same count as the input.  Returns 0 for an invalid shape or w_bit.
+ */
+WQ_API size_t wq_packed_bytes(int K, int N, int w_bit);
+
+/*
+ * wq_pack -- repack weights once, offline, into the tiled layout wq_matmul reads.
+ *
+ * q_in, w_bit 2 or 4: int32 (K / pack_num, N), pack_num = 32 / w_bit, in the
+ *   layout of BitDistiller quant_matmul_kernel (field k % pack_num of word
+ *   [k / pack_num][n], least significant field first).
+ * q_in, w_bit 8: int8 (N, K), K contiguous, as in tiny-llm int8_matmul.
+ * packed_out: wq_packed_bytes(K, N, w_bit) bytes.  The result is a pure bit
+ *   permutation of the input (bit-exact and invertible by wq_unpack): chunk
+ *   rows of KC = wq_chunk_k(w_bit) values along K, each holding N/16 tiles of
+ *   16 output channels x KC, 512 bytes per tile, ordered so that one 16-byte
+ *   load per thread of a warp yields whole tensor-core A fragments.
+ * Requirements: N % 16 == 0, K % KC == 0, both > 0; both pointers 16-byte
+ *   aligned; q_in and packed_out must not overlap.
+ */
+WQ_API wq_status wq_pack(const void *q_in, int K, int N, int w_bit, void *packed_out, void *stream);
+
+/*
+ * wq_unpack -- inverse of wq_pack for tests and tooling.
+ * codes_out: uint8 (K, N) row-major; code of (k, n) for w_bit 2/4, and the
+ *   two's-complement byte of q[n, k] for w_bit 8.
+ */
+WQ_API wq_status wq_unpack(const void *packed, int K, int N, int w_bit, uint8_t *codes_out, void *stream);
+
+/*
+ * Bytes of scratch memory wq_matmul needs for this problem (0 if none).
+ * The workspace holds fp32 partial sums of a split along K and one int32
+ * arrival counter per column block.  It must be zero-filled before its first
+ * use; every completed call leaves the counters at zero again, so one
+ * zero-fill at allocation is enough.  Calls that share a workspace must not
+ * run concurrently (they would race on the counters and partials).
+ */
+WQ_API size_t wq_workspace_bytes(int M, int N, int K, int w_bit, int group_size);
+
+/*
+ * wq_matmul -- y = x * dequant(W), fp32 accumulation, fp32 output.
+ *
+ * x        (M, K) row-major, x_dtype WQ_F16 or WQ_BF16.
+ * packed_w output of wq_pack for the same (K, N, w_bit).
+ * scales   w_bit 2/4: (K / group_size, N), s_dtype WQ_F16 or WQ_BF16.
+ *          w_bit 8:   (N,), s_dtype WQ_F32.
+ * zeros    w_bit 2/4: int32 (ceil(G / pack_num), N), G = K / group_size, zero
+ *          of group g in field g % pack_num of word [g / pack_num][n] (packed
+ *          along the group axis like the weights along K); NULL selects the
+ *          symmetric case, zero = 2^(w_bit - 1).  Unused high fields of the
+ *          last row are ignored.  w_bit 8: must be NULL (zero is 0, codes signed).
+ * group_size  w_bit 2/4: divides K, multiple of 16; -1 or K means one group per
+ *          column.  w_bit 8: ignored (per output channel).
+ * out      (M, N) fp32, fully overwritten.
+ * workspace / workspace_bytes: see wq_workspace_bytes (may be NULL/0 when it returns 0).
+ *
+ * M == 0 or N == 0 (with valid pointers) is a no-op returning WQ_OK, like the
+ * early return of Marlin's host launcher.  K == 0 is WQ_ERR_SHAPE.
+ * Precision: the weight codes and zeros enter the tensor cores exactly; the
+ * group scale and zero are applied to the fp32 partial sum of each group (small
+ * M) or to the weight, rounded once to the x dtype (large M).
+ */
+WQ_API wq_status wq_matmul(const void *x, wq_dtype x_dtype, const void *packed_w,
+                    const void *scales, wq_dtype s_dtype, const int32_t *zeros,
+                    int M, int N, int K, int w_bit, int group_size,
+                    float *out, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * wq_check_device -- synchronise `stream`, then read and clear the device
+ * word in which kernels record a barrier wait that gave up.  Returns
+ * WQ_ERR_TIMEOUT if one did, WQ_ERR_CUDA on a runtime error, else WQ_OK.
+ */
+WQ_API wq_status wq_check_device(void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* WQ_H */

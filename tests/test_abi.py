@@ -1,0 +1,100 @@
+"""The C ABI without a GPU: the library loads, exports every entry point that
+include/wq.h declares, and rejects invalid arguments on the host before it
+touches a device.  Only arguments that fail validation are passed, with
+placeholder pointers that are never dereferenced."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from weight_only_quantized_wq_gb300 import binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+FAKE = 0x10000  # 16-byte aligned placeholder, never dereferenced (validation fails first)
+
+
+@pytest.fixture(scope="module")
+def L():
+    from weight_only_quantized_wq_gb300 import build
+    build.build()
+    return binding.lib()
+
+
+def declared():
+    src = open(os.path.join(ROOT, "include", "wq.h")).read()
+    return re.findall(r"WQ_API[^;(]*?\b(wq_\w+)\s*\(", src)
+
+
+def test_header_declares_expected_entry_points():
+    assert set(declared()) == set(binding.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in declared():
+        assert hasattr(L, name), name
+        assert isinstance(getattr(L, name), ctypes._CFuncPtr)
+
+
+def test_status_strings(L):
+    for i in range(len(binding.STATUS)):
+        assert binding.wq_status_string(i)
+    assert binding.wq_status_string(99) == "unknown status"
+
+
+def test_sizes(L):
+    assert binding.wq_chunk_k(4) == 64 and binding.wq_chunk_k(2) == 128 and binding.wq_chunk_k(8) == 32
+    assert binding.wq_chunk_k(3) == 0
+    assert binding.wq_packed_bytes(4096, 11008, 4) == 4096 * 11008 // 2
+    assert binding.wq_packed_bytes(8192, 8192, 2) == 8192 * 8192 // 4
+    assert binding.wq_packed_bytes(4096, 4096, 8) == 4096 * 4096
+    assert binding.wq_packed_bytes(100, 64, 4) == 0   # K not a multiple of 64
+    assert binding.wq_packed_bytes(64, 20, 4) == 0    # N not a multiple of 16
+    assert binding.wq_packed_bytes(64, 16, 3) == 0
+
+
+def _mm(L, **kw):
+    a = dict(x=FAKE, xd=1, w=FAKE, s=FAKE, sd=1, z=None, M=4, N=64, K=128, wb=4, gs=64, out=FAKE, ws=None, wsb=0)
+    a.update(kw)
+    return L.wq_matmul(a["x"], a["xd"], a["w"], a["s"], a["sd"], a["z"], a["M"], a["N"], a["K"], a["wb"], a["gs"],
+                       a["out"], a["ws"], a["wsb"], None)
+
+
+def test_matmul_host_validation(L):
+    S = {n: i for i, n in enumerate(binding.STATUS)}
+    assert _mm(L, x=None) == S["WQ_ERR_NULL"]
+    assert _mm(L, out=None) == S["WQ_ERR_NULL"]
+    assert _mm(L, wb=3) == S["WQ_ERR_WBIT"]
+    assert _mm(L, K=0) == S["WQ_ERR_SHAPE"]
+    assert _mm(L, M=-1) == S["WQ_ERR_SHAPE"]
+    assert _mm(L, N=40) == S["WQ_ERR_SHAPE"]
+    assert _mm(L, K=96) == S["WQ_ERR_SHAPE"]
+    assert _mm(L, xd=2) == S["WQ_ERR_DTYPE"]
+    assert _mm(L, sd=2) == S["WQ_ERR_DTYPE"]
+    assert _mm(L, wb=8, sd=1) == S["WQ_ERR_DTYPE"]
+    assert _mm(L, wb=8, sd=2, z=FAKE) == S["WQ_ERR_DTYPE"]
+    assert _mm(L, gs=48) == S["WQ_ERR_GROUP"]
+    assert _mm(L, gs=8) == S["WQ_ERR_GROUP"]
+    assert _mm(L, gs=0) == S["WQ_ERR_GROUP"]
+    assert _mm(L, x=FAKE + 8) == S["WQ_ERR_ALIGN"]
+    assert _mm(L, out=FAKE + 4) == S["WQ_ERR_ALIGN"]
+    assert _mm(L, w=FAKE + 2) == S["WQ_ERR_ALIGN"]
+    # M == 0 and N == 0 are no-ops that succeed without touching a device
+    assert _mm(L, M=0) == S["WQ_OK"]
+    assert _mm(L, N=0) == S["WQ_OK"]
+
+
+def test_pack_host_validation(L):
+    S = {n: i for i, n in enumerate(binding.STATUS)}
+    assert L.wq_pack(None, 64, 16, 4, FAKE, None) == S["WQ_ERR_NULL"]
+    assert L.wq_pack(FAKE, 64, 16, 5, FAKE, None) == S["WQ_ERR_WBIT"]
+    assert L.wq_pack(FAKE, 60, 16, 4, FAKE, None) == S["WQ_ERR_SHAPE"]
+    assert L.wq_pack(FAKE, 64, 8, 4, FAKE, None) == S["WQ_ERR_SHAPE"]
+    assert L.wq_pack(FAKE + 4, 64, 16, 4, FAKE, None) == S["WQ_ERR_ALIGN"]
+    assert L.wq_unpack(FAKE, 64, 16, 4, None, None) == S["WQ_ERR_NULL"]
+    assert L.wq_unpack(FAKE, 0, 16, 4, FAKE, None) == S["WQ_ERR_SHAPE"]
+
+
+def test_workspace_bytes_invalid_is_zero(L):
+    assert binding.wq_workspace_bytes(0, 64, 128, 4, 64) == 0
+    assert binding.wq_workspace_bytes(4, 64, 100, 4, 64) == 0

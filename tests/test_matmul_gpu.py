@@ -1,0 +1,141 @@
+"""wq_matmul on the GPU against the fp64 CPU oracle.
+
+- every workload of the statement of the problem at its full size (the large
+  prefill sweep on sampled rows), within max|err| <= 1e-2 sqrt(K/4096) RMS;
+- integer-exact inputs (x integer in [-4, 4], scales 2^-4) where every fp32
+  sum is exact in any order: the GPU must equal the oracle bit for bit;
+- the symmetric path against the asymmetric one with every zero 8;
+- determinism, ragged shapes, the M == 0 no-op, and canaries past the output.
+"""
+import numpy as np
+import pytest
+import torch
+
+import weight_only_quantized_wq_gb300 as wq
+from weight_only_quantized_wq_gb300 import synthetic as syn
+from tests.helpers import assert_close, oracle_y, run, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("make", [syn.int4_asym_tiny, syn.int8_per_channel, syn.int4_sym_decode, syn.int2_asym],
+                         ids=["int4_asym_tiny", "int8_per_channel", "int4_sym_decode", "int2_asym"])
+def test_workload_full_output(make):
+    p = make()
+    y = run(p).cpu().numpy()
+    assert_close(y, oracle_y(p), p.K, p.name)
+
+
+_SWEEP = {}
+
+
+def _sweep():
+    if "p" not in _SWEEP:
+        _SWEEP["p"] = syn.int4_asym_sweep(4096)
+        _SWEEP["d"] = to_device(_SWEEP["p"])
+    return _SWEEP["p"], _SWEEP["d"]
+
+
+@pytest.mark.parametrize("M", syn.C5_MS)
+def test_prefill_sweep_sampled_rows(M):
+    full, d = _sweep()
+    p = full.rows(M)
+    dd = dict(d, x=d["x"][:M].contiguous())
+    y = run(p, dd).cpu().numpy()
+    rng = np.random.default_rng(M)
+    rows = sorted(set([0, M - 1] + rng.choice(M, size=min(M, 14), replace=False).tolist()))
+    ref = oracle_y(p, rows=rows)
+    assert_close(y[rows], ref, p.K, p.name)
+    assert np.all(np.isfinite(y))
+
+
+INT_EXACT = [  # (name, M, K, N, w_bit, group, x, s, symmetric)
+    ("int4-asym-f16", 1, 512, 512, 4, 128, "f16", "f16", False),
+    ("int4-sym-f16", 3, 4096, 1024, 4, 128, "f16", "f16", True),
+    ("int2-asym-bf16", 8, 8192, 1024, 2, 64, "bf16", "bf16", False),
+    ("int4-asym-bf16-M16", 16, 8192, 2048, 4, 128, "bf16", "bf16", False),
+    ("int4-asym-bf16-M64", 64, 1024, 512, 4, 128, "bf16", "bf16", False),
+    ("int4-perchannel-bf16", 5, 2048, 256, 4, 2048, "bf16", "bf16", False),
+    ("int2-g32-f16", 2, 1024, 128, 2, 32, "f16", "bf16", False),
+]
+
+
+@pytest.mark.parametrize("case", INT_EXACT, ids=[c[0] for c in INT_EXACT])
+def test_integer_exact_bitwise(case):
+    name, M, K, N, wb, gs, xd, sd, sym = case
+    p = syn.grouped(name, M, K, N, wb, gs, xd, sd, (0, 0), symmetric=sym, seed=11, int_exact=True)
+    y = run(p).cpu().numpy().astype(np.float64)
+    ref = oracle_y(p)
+    assert np.array_equal(y, ref), "max diff %g" % np.max(np.abs(y - ref))
+
+
+def test_int8_integer_exact_bitwise():
+    p = syn.int8("int8-exact", 16, 4096, 1024, "bf16", (0.001, 0.01), seed=12, int_exact=True)
+    y = run(p).cpu().numpy().astype(np.float64)
+    ref = oracle_y(p)
+    # the sum is exact; one fp32 multiply by the scale, correctly rounded
+    assert np.array_equal(y, ref.astype(np.float32).astype(np.float64))
+
+
+def test_symmetric_equals_zero8():
+    p = syn.int4_sym_decode()
+    d = to_device(p)
+    ys = run(p, d)
+    G = p.K // p.group_size
+    z8 = torch.full(((G + 7) // 8, p.N), 0x88888888 - 2 ** 32, dtype=torch.int32, device="cuda")
+    ya = wq.wq_matmul(d["x"], d["packed"], d["scales"], z8, p.M, p.N, p.K, 4, p.group_size)
+    assert torch.equal(ys, ya)
+
+
+def test_deterministic():
+    for make in (syn.int4_sym_decode, syn.int2_asym, syn.int8_per_channel):
+        p = make()
+        d = to_device(p)
+        assert torch.equal(run(p, d), run(p, d))
+
+
+RAGGED = [  # (M, K, N, w_bit, group) -- tails of token tiles, CTA column blocks, splits, groups
+    (3, 256, 80, 4, 64), (13, 512, 48, 4, 128), (17, 1024, 272, 2, 64), (33, 512, 208, 4, 32),
+    (65, 256, 64, 4, 256), (100, 512, 144, 4, 128), (7, 4096, 16, 4, 128), (2, 8192, 32, 2, 128),
+    (40, 640, 96, 8, 640), (1, 32, 16, 8, 32), (9, 64, 16, 4, 16),
+]
+
+
+@pytest.mark.parametrize("M,K,N,wb,gs", RAGGED)
+def test_ragged_shapes(M, K, N, wb, gs):
+    if wb == 8:
+        p = syn.int8("int8-ragged", M, K, N, "bf16", (0.001, 0.01), seed=M + K)
+    else:
+        p = syn.grouped("ragged", M, K, N, wb, gs, "bf16" if M % 2 else "f16", "bf16", (0.005, 0.02),
+                        seed=M + K + N)
+    y = run(p).cpu().numpy()
+    assert_close(y, oracle_y(p), K, "ragged %s" % ((M, K, N, wb, gs),))
+
+
+def test_zero_rows_is_noop_and_canaries():
+    p = syn.int4_asym_tiny()
+    d = to_device(p)
+    out = torch.full((p.N + 64,), float("nan"), device="cuda")
+    wq.wq_matmul(d["x"], d["packed"], d["scales"], d["zeros"], 0, p.N, p.K, 4, 128, out=out[:p.N].view(0, p.N))
+    torch.cuda.synchronize()
+    assert torch.isnan(out).all()
+    # one row written, the guard band after it untouched
+    sentinel = -12345.0
+    buf = torch.full((p.N + 64,), sentinel, device="cuda")
+    wq.wq_matmul(d["x"], d["packed"], d["scales"], d["zeros"], 1, p.N, p.K, 4, 128, out=buf[:p.N].view(1, p.N))
+    torch.cuda.synchronize()
+    assert bool((buf[p.N:] == sentinel).all())
+    assert not bool((buf[:p.N] == sentinel).any())
+    wq.wq_check_device()
+
+
+def test_workspace_too_small_is_rejected():
+    p = syn.int4_sym_decode()
+    need = wq.wq_workspace_bytes(p.M, p.N, p.K, 4, p.group_size)
+    if need == 0:
+        pytest.skip("this shape needs no workspace on this GPU")
+    d = to_device(p)
+    small = torch.zeros(need - 16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(wq.WQError) as e:
+        wq.wq_matmul(d["x"], d["packed"], d["scales"], None, p.M, p.N, p.K, 4, p.group_size, workspace=small)
+    assert e.value.status == 7

@@ -1,0 +1,149 @@
+"""ctypes binding of libwq (include/wq.h): argument marshalling only.
+
+Every function here forwards to the C entry point of the same name.  torch is
+used for device memory and the current CUDA stream, nothing else; all the
+arithmetic runs in the library's CUDA kernels.  If libwq.so is missing the
+import fails -- there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libwq.so")
+
+WQ_F16, WQ_BF16, WQ_F32 = 0, 1, 2
+_DTYPE = {torch.float16: WQ_F16, torch.bfloat16: WQ_BF16, torch.float32: WQ_F32}
+
+STATUS = ["WQ_OK", "WQ_ERR_NULL", "WQ_ERR_SHAPE", "WQ_ERR_WBIT", "WQ_ERR_GROUP", "WQ_ERR_DTYPE",
+          "WQ_ERR_ALIGN", "WQ_ERR_WORKSPACE", "WQ_ERR_ARCH", "WQ_ERR_CUDA", "WQ_ERR_TIMEOUT"]
+
+EXPORTS = ("wq_status_string", "wq_chunk_k", "wq_packed_bytes", "wq_pack", "wq_unpack",
+           "wq_workspace_bytes", "wq_matmul", "wq_check_device")
+
+
+class WQError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        name = STATUS[status] if 0 <= status < len(STATUS) else str(status)
+        super().__init__("%s: %s (%s)" % (what, name, wq_status_string(status)))
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libwq.so (built by weight_only_quantized_wq_gb300.build)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise ImportError("libwq.so is not built (run weight_only_quantized_wq_gb300.build.build())")
+        L = ctypes.CDLL(_LIB_PATH)
+        P, I, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+        L.wq_status_string.restype = ctypes.c_char_p
+        L.wq_status_string.argtypes = [I]
+        L.wq_chunk_k.restype = I
+        L.wq_chunk_k.argtypes = [I]
+        L.wq_packed_bytes.restype = Z
+        L.wq_packed_bytes.argtypes = [I, I, I]
+        L.wq_pack.restype = I
+        L.wq_pack.argtypes = [P, I, I, I, P, P]
+        L.wq_unpack.restype = I
+        L.wq_unpack.argtypes = [P, I, I, I, P, P]
+        L.wq_workspace_bytes.restype = Z
+        L.wq_workspace_bytes.argtypes = [I, I, I, I, I]
+        L.wq_matmul.restype = I
+        L.wq_matmul.argtypes = [P, I, P, P, I, P, I, I, I, I, I, P, P, Z, P]
+        L.wq_check_device.restype = I
+        L.wq_check_device.argtypes = [P]
+        _lib = L
+    return _lib
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(st: int, what: str):
+    if st != 0:
+        raise WQError(st, what)
+
+
+def wq_status_string(status: int) -> str:
+    return lib().wq_status_string(int(status)).decode()
+
+
+def wq_chunk_k(w_bit: int) -> int:
+    return lib().wq_chunk_k(int(w_bit))
+
+
+def wq_packed_bytes(K: int, N: int, w_bit: int) -> int:
+    return lib().wq_packed_bytes(K, N, w_bit)
+
+
+def wq_pack(q_in: torch.Tensor, K: int, N: int, w_bit: int, packed_out: torch.Tensor | None = None,
+            stream=None) -> torch.Tensor:
+    """Repack page-layout weights (int32 (K/pack, N), or int8 (N, K) for w_bit 8)
+    into the tiled layout; returns the uint8 packed buffer."""
+    if packed_out is None:
+        n = wq_packed_bytes(K, N, w_bit)
+        packed_out = torch.empty(max(n, 16), dtype=torch.uint8, device=q_in.device)
+    _check(lib().wq_pack(_ptr(q_in), K, N, w_bit, _ptr(packed_out), _stream(stream)), "wq_pack")
+    return packed_out
+
+
+def wq_unpack(packed: torch.Tensor, K: int, N: int, w_bit: int, codes_out: torch.Tensor | None = None,
+              stream=None) -> torch.Tensor:
+    """Inverse of wq_pack: uint8 codes (K, N)."""
+    if codes_out is None:
+        codes_out = torch.empty((K, N), dtype=torch.uint8, device=packed.device)
+    _check(lib().wq_unpack(_ptr(packed), K, N, w_bit, _ptr(codes_out), _stream(stream)), "wq_unpack")
+    return codes_out
+
+
+def wq_workspace_bytes(M: int, N: int, K: int, w_bit: int, group_size: int) -> int:
+    return lib().wq_workspace_bytes(M, N, K, w_bit, group_size)
+
+
+_workspaces: dict = {}
+
+
+def workspace_for(M, N, K, w_bit, group_size, device) -> torch.Tensor | None:
+    """A zero-filled workspace big enough for this problem, cached per device.
+    Completed calls leave it reusable (its counters back at zero)."""
+    need = wq_workspace_bytes(M, N, K, w_bit, group_size)
+    if need == 0:
+        return None
+    key = torch.device(device).index
+    ws = _workspaces.get(key)
+    if ws is None or ws.numel() < need:
+        ws = torch.zeros(need, dtype=torch.uint8, device=device)
+        _workspaces[key] = ws
+    return ws
+
+
+def wq_matmul(x: torch.Tensor, packed_w: torch.Tensor, scales: torch.Tensor, zeros: torch.Tensor | None,
+              M: int, N: int, K: int, w_bit: int, group_size: int, out: torch.Tensor | None = None,
+              workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """y (M, N) fp32 = x @ dequant(W) through the C entry point wq_matmul."""
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    if workspace is None:
+        workspace = workspace_for(M, N, K, w_bit, group_size, x.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib().wq_matmul(_ptr(x), _DTYPE.get(x.dtype, -1), _ptr(packed_w), _ptr(scales),
+                         _DTYPE.get(scales.dtype, -1), _ptr(zeros), M, N, K, w_bit, group_size,
+                         _ptr(out), _ptr(workspace), ws_bytes, _stream(stream))
+    _check(st, "wq_matmul")
+    return out
+
+
+def wq_check_device(stream=None) -> None:
+    _check(lib().wq_check_device(_stream(stream)), "wq_check_device")

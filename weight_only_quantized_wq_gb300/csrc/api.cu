@@ -1,0 +1,195 @@
+// api.cu -- the C ABI declared in include/wq.h: host-side validation, the
+// per-device cache, and dispatch to the kernels.  No entry point allocates
+// device memory or synchronises (wq_check_device excepted).
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cuda_runtime.h>
+
+#include "kernels.h"
+#include "wq.h"
+
+namespace {
+
+// Device status word: kernels OR bits into it when a barrier wait gives up.
+__device__ uint32_t g_status_word;
+
+struct DeviceInfo {
+  bool ready = false;
+  bool arch_ok = false;
+  int sms = 0;
+  uint32_t *status = nullptr;  // device address of g_status_word on this device
+};
+
+constexpr int kMaxDevices = 64;
+DeviceInfo g_devices[kMaxDevices];
+std::mutex g_mutex;
+
+// Query (once per device) the SM count, the architecture, and the device
+// address of the status word.  Must run with that device current.
+wq_status device_info(DeviceInfo **out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return WQ_ERR_CUDA;
+  DeviceInfo &d = g_devices[dev];
+  if (!d.ready) {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (!d.ready) {
+      int major = 0, minor = 0, sms = 0;
+      if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+          cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+          cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return WQ_ERR_CUDA;
+      d.arch_ok = (major == 10 && minor == 3);
+      d.sms = sms;
+      if (d.arch_ok) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return WQ_ERR_CUDA;
+        d.status = static_cast<uint32_t *>(p);
+      }
+      d.ready = true;
+    }
+  }
+  if (!d.arch_ok) return WQ_ERR_ARCH;
+  *out = &d;
+  return WQ_OK;
+}
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool valid_wbit(int w) { return w == 2 || w == 4 || w == 8; }
+
+// Shape rules shared by pack, unpack and matmul.
+wq_status check_kn(int K, int N, int w_bit) {
+  if (!valid_wbit(w_bit)) return WQ_ERR_WBIT;
+  if (K <= 0 || N <= 0) return WQ_ERR_SHAPE;
+  if (N % 16 != 0 || K % (256 / w_bit) != 0) return WQ_ERR_SHAPE;
+  return WQ_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *wq_status_string(wq_status s) {
+  switch (s) {
+    case WQ_OK: return "ok";
+    case WQ_ERR_NULL: return "a required pointer is NULL";
+    case WQ_ERR_SHAPE: return "invalid or unsupported shape (need N % 16 == 0, K % (256 / w_bit) == 0)";
+    case WQ_ERR_WBIT: return "w_bit must be 2, 4 or 8";
+    case WQ_ERR_GROUP: return "group_size must divide K and be a multiple of 16 (or -1 / K)";
+    case WQ_ERR_DTYPE: return "unsupported dtype combination";
+    case WQ_ERR_ALIGN: return "pointer not aligned (x, weights, out: 16 bytes)";
+    case WQ_ERR_WORKSPACE: return "workspace missing or smaller than wq_workspace_bytes()";
+    case WQ_ERR_ARCH: return "current device is not compute capability 10.3 (sm_103a)";
+    case WQ_ERR_CUDA: return "CUDA runtime error";
+    case WQ_ERR_TIMEOUT: return "a kernel gave up waiting on one of its barriers";
+  }
+  return "unknown status";
+}
+
+int wq_chunk_k(int w_bit) { return valid_wbit(w_bit) ? 256 / w_bit : 0; }
+
+size_t wq_packed_bytes(int K, int N, int w_bit) {
+  if (check_kn(K, N, w_bit) != WQ_OK) return 0;
+  return (size_t)K * N * w_bit / 8;
+}
+
+wq_status wq_pack(const void *q_in, int K, int N, int w_bit, void *packed_out, void *stream) {
+  if (!q_in || !packed_out) return WQ_ERR_NULL;
+  wq_status st = check_kn(K, N, w_bit);
+  if (st != WQ_OK) return st;
+  if (!aligned(q_in, 16) || !aligned(packed_out, 16)) return WQ_ERR_ALIGN;
+  DeviceInfo *d = nullptr;
+  if ((st = device_info(&d)) != WQ_OK) return st;
+  return wq::launch_pack(q_in, packed_out, K, N, w_bit, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? WQ_OK
+             : WQ_ERR_CUDA;
+}
+
+wq_status wq_unpack(const void *packed, int K, int N, int w_bit, uint8_t *codes_out, void *stream) {
+  if (!packed || !codes_out) return WQ_ERR_NULL;
+  wq_status st = check_kn(K, N, w_bit);
+  if (st != WQ_OK) return st;
+  if (!aligned(packed, 16)) return WQ_ERR_ALIGN;
+  DeviceInfo *d = nullptr;
+  if ((st = device_info(&d)) != WQ_OK) return st;
+  return wq::launch_unpack(packed, codes_out, K, N, w_bit, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? WQ_OK
+             : WQ_ERR_CUDA;
+}
+
+size_t wq_workspace_bytes(int M, int N, int K, int w_bit, int group_size) {
+  (void)group_size;
+  if (M <= 0 || check_kn(K, N, w_bit) != WQ_OK) return 0;
+  DeviceInfo *d = nullptr;
+  if (device_info(&d) != WQ_OK) return 0;
+  return wq::plan_decode(M, N, K, w_bit, d->sms).workspace;
+}
+
+wq_status wq_matmul(const void *x, wq_dtype x_dtype, const void *packed_w, const void *scales, wq_dtype s_dtype,
+                    const int32_t *zeros, int M, int N, int K, int w_bit, int group_size, float *out,
+                    void *workspace, size_t workspace_bytes, void *stream) {
+  if (!x || !packed_w || !scales || !out) return WQ_ERR_NULL;
+  if (!valid_wbit(w_bit)) return WQ_ERR_WBIT;
+  if (M < 0 || N < 0 || K <= 0) return WQ_ERR_SHAPE;
+  if (M == 0 || N == 0) return WQ_OK;
+  wq_status st = check_kn(K, N, w_bit);
+  if (st != WQ_OK) return st;
+  if (x_dtype != WQ_F16 && x_dtype != WQ_BF16) return WQ_ERR_DTYPE;
+  if (w_bit == 8) {
+    if (s_dtype != WQ_F32 || zeros != nullptr) return WQ_ERR_DTYPE;
+    group_size = K;
+  } else {
+    if (s_dtype != WQ_F16 && s_dtype != WQ_BF16) return WQ_ERR_DTYPE;
+    if (group_size == -1) group_size = K;
+    if (group_size <= 0 || K % group_size != 0 || group_size % 16 != 0) return WQ_ERR_GROUP;
+  }
+  if (!aligned(x, 16) || !aligned(packed_w, 16) || !aligned(out, 16) ||
+      !aligned(scales, s_dtype == WQ_F32 ? 4 : 2) || !aligned(zeros, 4))
+    return WQ_ERR_ALIGN;
+  DeviceInfo *d = nullptr;
+  if ((st = device_info(&d)) != WQ_OK) return st;
+
+  const wq::DecodePlan plan = wq::plan_decode(M, N, K, w_bit, d->sms);
+  if (plan.workspace > 0) {
+    if (!workspace || workspace_bytes < plan.workspace) return WQ_ERR_WORKSPACE;
+    if (!aligned(workspace, 16)) return WQ_ERR_ALIGN;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  wq::MatmulArgs a{};
+  a.packed = packed_w;
+  a.scales = scales;
+  a.zeros = reinterpret_cast<const uint32_t *>(zeros);
+  a.N = N;
+  a.K = K;
+  a.w_bit = w_bit;
+  a.group_size = group_size;
+  a.x_bf16 = (x_dtype == WQ_BF16);
+  a.s_bf16 = (s_dtype == WQ_BF16);
+  a.err = d->status;
+  // Rows are processed 64 at a time (the decode kernel's token tile).
+  for (int m0 = 0; m0 < M; m0 += 64) {
+    a.M = (M - m0) < 64 ? (M - m0) : 64;
+    a.x = static_cast<const uint16_t *>(x) + (size_t)m0 * K;
+    a.out = out + (size_t)m0 * N;
+    const wq::DecodePlan p = (M <= 64 || a.M == 64) ? plan : wq::plan_decode(a.M, N, K, w_bit, d->sms);
+    if (wq::launch_decode(a, p, workspace, s) != cudaSuccess) return WQ_ERR_CUDA;
+  }
+  return WQ_OK;
+}
+
+wq_status wq_check_device(void *stream) {
+  DeviceInfo *d = nullptr;
+  wq_status st = device_info(&d);
+  if (st != WQ_OK) return st;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return WQ_ERR_CUDA;
+  uint32_t v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_status_word, sizeof(v)) != cudaSuccess) return WQ_ERR_CUDA;
+  if (v == 0) return WQ_OK;
+  const uint32_t zero = 0;
+  if (cudaMemcpyToSymbol(g_status_word, &zero, sizeof(zero)) != cudaSuccess) return WQ_ERR_CUDA;
+  return WQ_ERR_TIMEOUT;
+}
+
+}  // extern "C"

@@ -1,0 +1,190 @@
+// dev.cuh -- device primitives shared by the libwq kernels (sm_103a).
+//
+// Hand-written PTX wrappers: mbarriers with time-bounded waits, 1-D bulk
+// copies (cp.async.bulk, no multicast), warp-level tensor-core MMA, and the
+// bit tricks that turn packed integer codes into fp16/bf16 operands.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace wq {
+
+// Bits recorded in the library's device status word.
+constexpr uint32_t kDevErrTimeout = 1u;
+
+// A barrier wait gives up after this many nanoseconds of wall-clock time.
+constexpr uint64_t kWaitLimitNs = 4000000000ull;
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// ---------------------------------------------------------------- mbarrier
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+// Make barrier initialisation visible to the async proxy (bulk copies, tensor core).
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for the phase of `bar` with the given parity to complete.  Gives up
+// after kWaitLimitNs, records kDevErrTimeout in *err and returns false.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t *err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 255u) == 0u && global_timer_ns() - t0 > kWaitLimitNs) {
+      atomicOr(err, kDevErrTimeout);
+      return false;
+    }
+  }
+}
+
+// ---------------------------------------------------------------- bulk copy
+// L2 policy: weights are read exactly once per call; let them go first.
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// 1-D bulk copy global -> this CTA's shared memory, completing `bytes` of
+// transaction count on `bar`.  dst, src 16-byte aligned; bytes % 16 == 0.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar,
+                                         uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1], %2, [%3], %4;" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+// ---------------------------------------------------------------- loads
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint2 lds64(uint32_t a) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+  return v;
+}
+
+// ---------------------------------------------------------------- MMA
+// D += A * B, m16n8k16, fp32 accumulate.  A row-major 16x16 (4 regs), B
+// column-major 16x8 (2 regs), C/D 16x8 fp32 (4 regs).
+template <bool BF16>
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  if constexpr (BF16) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  } else {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  }
+}
+
+// ---------------------------------------------------------------- dequant
+// (a & b) | c as one LOP3.
+__device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+// Magic-exponent conversion.  A float whose exponent makes the unit in the
+// last place exactly 1 turns an integer u written into its low mantissa bits
+// into the value MAGIC + u, exactly: 1024 + u for fp16 (10 fraction bits),
+// 128 + u for bf16 (7 fraction bits).  Two values per 32-bit register.
+template <bool BF16>
+struct Magic {
+  static constexpr uint32_t kPair = BF16 ? 0x43004300u : 0x64006400u;  // (128, 128) or (1024, 1024)
+  static constexpr float kValue = BF16 ? 128.0f : 1024.0f;
+  static constexpr uint32_t kOnePair = BF16 ? 0x3F803F80u : 0x3C003C00u;  // (1.0, 1.0)
+};
+
+// Pair i of a packed word: fields i and i + 32/(2*W_BIT) land in the low and
+// high 16-bit halves as (MAGIC + code).  W_BIT 2 or 4.
+template <int W_BIT, bool BF16>
+__device__ __forceinline__ uint32_t code_pair(uint32_t w, int i) {
+  constexpr uint32_t mask = W_BIT == 4 ? 0x000F000Fu : 0x00030003u;
+  return and_or(w >> (W_BIT * i), mask, Magic<BF16>::kPair);
+}
+
+// Signed int8 bytes (lo, hi) of a word -> exact fp16/bf16 pair.
+template <bool BF16>
+__device__ __forceinline__ uint32_t int8_pair(uint32_t w, int hi_half) {
+  const uint32_t u = w ^ 0x80808080u;  // unsigned u = q + 128 per byte
+  if constexpr (BF16) {
+    // 0x4B0000uu is the fp32 value 2^23 + u; subtract 2^23 + 128.
+    const uint32_t s0 = hi_half ? 0x7442u : 0x7440u;
+    const uint32_t s1 = hi_half ? 0x7443u : 0x7441u;
+    const float f0 = __uint_as_float(__byte_perm(u, 0x4B000000u, s0)) - 8388736.0f;
+    const float f1 = __uint_as_float(__byte_perm(u, 0x4B000000u, s1)) - 8388736.0f;
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(f1), "f"(f0));  // high <- f1, low <- f0
+    return r;
+  } else {
+    // 0x64uu is the fp16 value 1024 + u; subtract 1152 from both halves.
+    const uint32_t h = __byte_perm(u, 0x64646464u, hi_half ? 0x7362u : 0x5140u);
+    uint32_t r;
+    asm("sub.f16x2 %0, %1, %2;" : "=r"(r) : "r"(h), "r"(0x64806480u));
+    return r;
+  }
+}
+
+__device__ __forceinline__ float half_bits_to_float(uint16_t h, bool bf16) {
+  if (bf16) return __uint_as_float(static_cast<uint32_t>(h) << 16);
+  float f;
+  asm("cvt.f32.f16 %0, %1;" : "=f"(f) : "h"(h));
+  return f;
+}
+
+}  // namespace wq

@@ -1,0 +1,40 @@
+// kernels.h -- internal launchers shared between the kernel files and the C ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace wq {
+
+cudaError_t launch_pack(const void *qin, void *out, int K, int N, int w_bit, cudaStream_t s);
+cudaError_t launch_unpack(const void *packed, uint8_t *codes, int K, int N, int w_bit, cudaStream_t s);
+
+// Problem handed to the matmul kernels after host validation.
+struct MatmulArgs {
+  const void *x;          // (M, K) f16/bf16
+  const void *packed;     // wq_pack layout
+  const void *scales;     // (G, N) f16/bf16, or (N,) f32 for int8
+  const uint32_t *zeros;  // (ceil(G/V), N) or nullptr
+  float *out;             // (M, N)
+  int M, N, K, w_bit, group_size;
+  bool x_bf16, s_bf16;
+  uint32_t *err;          // device status word
+};
+
+// Split of the decode kernel over the GPU, chosen on the host.
+struct DecodePlan {
+  int mt;        // 8-row token tiles (1, 2, 4, 8)
+  int tn;        // 16-row weight tiles per warp
+  int nblocks;   // CTAs along N
+  int splits;    // CTAs along K
+  int cps;       // chunk rows per split
+  size_t workspace;  // bytes: counters, then splits * M * N fp32 partials (0 if splits == 1)
+};
+
+size_t decode_counter_bytes(int N);
+
+DecodePlan plan_decode(int M, int N, int K, int w_bit, int sms);
+cudaError_t launch_decode(const MatmulArgs &a, const DecodePlan &p, void *workspace, cudaStream_t s);
+
+}  // namespace wq
