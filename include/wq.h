@@ -94,8 +94,8 @@ WQ_API size_t wq_packed_bytes(int K, int N, int w_bit);
  *   rows of KC = wq_chunk_k(w_bit) values along K, each holding N/16 tiles of
  *   16 output channels x KC, 512 bytes per tile, ordered so that one 16-byte
  *   load per thread of a warp yields whole tensor-core A fragments.
- * Requirements: N % 16 == 0, K % KC == 0, both > 0; both pointers 16-byte
- *   aligned; q_in and packed_out must not overlap.
+ * Requirements: N % 16 == 0, N <= 262144, K % KC == 0, both > 0; both
+ *   pointers 16-byte aligned; q_in and packed_out must not overlap.
  */
 WQ_API wq_status wq_pack(const void *q_in, int K, int N, int w_bit, void *packed_out, void *stream);
 
@@ -108,10 +108,11 @@ WQ_API wq_status wq_unpack(const void *packed, int K, int N, int w_bit, uint8_t 
 
 /*
  * Bytes of scratch memory wq_matmul needs for this problem (0 if none).
- * The workspace holds fp32 partial sums of a split along K and one int32
- * arrival counter per column block.  It must be zero-filled before its first
- * use; every completed call leaves the counters at zero again, so one
- * zero-fill at allocation is enough.  Calls that share a workspace must not
+ * The workspace holds a fixed 16 KiB block of int32 arrival counters (one per
+ * column block) followed by the fp32 partial sums of a split along K.  It
+ * must be zero-filled before its first use; every completed call leaves the
+ * counters at zero again, so one zero-fill at allocation is enough for any
+ * later call, whatever its shape, as long as the buffer is large enough.  Calls that share a workspace must not
  * run concurrently (they would race on the counters and partials).
  */
 WQ_API size_t wq_workspace_bytes(int M, int N, int K, int w_bit, int group_size);
@@ -131,6 +132,7 @@ WQ_API size_t wq_workspace_bytes(int M, int N, int K, int w_bit, int group_size)
  * group_size  w_bit 2/4: divides K, multiple of 16; -1 or K means one group per
  *          column.  w_bit 8: ignored (per output channel).
  * out      (M, N) fp32, fully overwritten.
+ * x, packed_w, scales, zeros, out and workspace must be 16-byte aligned.
  * workspace / workspace_bytes: see wq_workspace_bytes (may be NULL/0 when it returns 0).
  *
  * M == 0 or N == 0 (with valid pointers) is a no-op returning WQ_OK, like the

@@ -63,7 +63,7 @@ bool valid_wbit(int w) { return w == 2 || w == 4 || w == 8; }
 wq_status check_kn(int K, int N, int w_bit) {
   if (!valid_wbit(w_bit)) return WQ_ERR_WBIT;
   if (K <= 0 || N <= 0) return WQ_ERR_SHAPE;
-  if (N % 16 != 0 || K % (256 / w_bit) != 0) return WQ_ERR_SHAPE;
+  if (N % 16 != 0 || K % (256 / w_bit) != 0 || N > wq::kMaxN) return WQ_ERR_SHAPE;
   return WQ_OK;
 }
 
@@ -75,11 +75,11 @@ const char *wq_status_string(wq_status s) {
   switch (s) {
     case WQ_OK: return "ok";
     case WQ_ERR_NULL: return "a required pointer is NULL";
-    case WQ_ERR_SHAPE: return "invalid or unsupported shape (need N % 16 == 0, K % (256 / w_bit) == 0)";
+    case WQ_ERR_SHAPE: return "invalid or unsupported shape (need N % 16 == 0, N <= 262144, K % (256 / w_bit) == 0)";
     case WQ_ERR_WBIT: return "w_bit must be 2, 4 or 8";
     case WQ_ERR_GROUP: return "group_size must divide K and be a multiple of 16 (or -1 / K)";
     case WQ_ERR_DTYPE: return "unsupported dtype combination";
-    case WQ_ERR_ALIGN: return "pointer not aligned (x, weights, out: 16 bytes)";
+    case WQ_ERR_ALIGN: return "pointer not 16-byte aligned";
     case WQ_ERR_WORKSPACE: return "workspace missing or smaller than wq_workspace_bytes()";
     case WQ_ERR_ARCH: return "current device is not compute capability 10.3 (sm_103a)";
     case WQ_ERR_CUDA: return "CUDA runtime error";
@@ -120,11 +120,11 @@ wq_status wq_unpack(const void *packed, int K, int N, int w_bit, uint8_t *codes_
 }
 
 size_t wq_workspace_bytes(int M, int N, int K, int w_bit, int group_size) {
-  (void)group_size;
   if (M <= 0 || check_kn(K, N, w_bit) != WQ_OK) return 0;
   DeviceInfo *d = nullptr;
   if (device_info(&d) != WQ_OK) return 0;
-  return wq::plan_decode(M, N, K, w_bit, d->sms).workspace;
+  // The split (and so the workspace) does not depend on the zeros or the group size.
+  return wq::plan_decode(M, N, K, w_bit, group_size, true, d->sms).workspace;
 }
 
 wq_status wq_matmul(const void *x, wq_dtype x_dtype, const void *packed_w, const void *scales, wq_dtype s_dtype,
@@ -145,13 +145,12 @@ wq_status wq_matmul(const void *x, wq_dtype x_dtype, const void *packed_w, const
     if (group_size == -1) group_size = K;
     if (group_size <= 0 || K % group_size != 0 || group_size % 16 != 0) return WQ_ERR_GROUP;
   }
-  if (!aligned(x, 16) || !aligned(packed_w, 16) || !aligned(out, 16) ||
-      !aligned(scales, s_dtype == WQ_F32 ? 4 : 2) || !aligned(zeros, 4))
+  if (!aligned(x, 16) || !aligned(packed_w, 16) || !aligned(out, 16) || !aligned(scales, 16) || !aligned(zeros, 16))
     return WQ_ERR_ALIGN;
   DeviceInfo *d = nullptr;
   if ((st = device_info(&d)) != WQ_OK) return st;
 
-  const wq::DecodePlan plan = wq::plan_decode(M, N, K, w_bit, d->sms);
+  const wq::DecodePlan plan = wq::plan_decode(M, N, K, w_bit, group_size, zeros != nullptr, d->sms);
   if (plan.workspace > 0) {
     if (!workspace || workspace_bytes < plan.workspace) return WQ_ERR_WORKSPACE;
     if (!aligned(workspace, 16)) return WQ_ERR_ALIGN;
@@ -173,7 +172,8 @@ wq_status wq_matmul(const void *x, wq_dtype x_dtype, const void *packed_w, const
     a.M = (M - m0) < 64 ? (M - m0) : 64;
     a.x = static_cast<const uint16_t *>(x) + (size_t)m0 * K;
     a.out = out + (size_t)m0 * N;
-    const wq::DecodePlan p = (M <= 64 || a.M == 64) ? plan : wq::plan_decode(a.M, N, K, w_bit, d->sms);
+    const wq::DecodePlan p =
+        (M <= 64 || a.M == 64) ? plan : wq::plan_decode(a.M, N, K, w_bit, group_size, zeros != nullptr, d->sms);
     if (wq::launch_decode(a, p, workspace, s) != cudaSuccess) return WQ_ERR_CUDA;
   }
   return WQ_OK;

@@ -29,12 +29,17 @@ struct DecodePlan {
   int nblocks;   // CTAs along N
   int splits;    // CTAs along K
   int cps;       // chunk rows per split
+  int gcap;      // most groups one chunk row touches (scale / zero rows per stage)
+  int stage_bytes;
   size_t workspace;  // bytes: counters, then splits * M * N fp32 partials (0 if splits == 1)
 };
 
-size_t decode_counter_bytes(int N);
+// Arrival counters at the start of every workspace (one per column block).
+constexpr int kMaxColumnBlocks = 4096;
+constexpr int kMaxN = 16 * 4 * kMaxColumnBlocks;  // 262144 output channels
+size_t decode_counter_bytes();
 
-DecodePlan plan_decode(int M, int N, int K, int w_bit, int sms);
+DecodePlan plan_decode(int M, int N, int K, int w_bit, int group_size, bool zero, int sms);
 cudaError_t launch_decode(const MatmulArgs &a, const DecodePlan &p, void *workspace, cudaStream_t s);
 
 }  // namespace wq
