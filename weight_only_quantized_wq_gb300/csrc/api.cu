@@ -167,7 +167,13 @@ wq_status wq_matmul(const void *x, wq_dtype x_dtype, const void *packed_w, const
   a.x_bf16 = (x_dtype == WQ_BF16);
   a.s_bf16 = (s_dtype == WQ_BF16);
   a.err = d->status;
-  // Rows are processed 64 at a time (the decode kernel's token tile).
+  if (M >= wq::kPrefillMinM) {
+    a.M = M;
+    a.x = x;
+    a.out = out;
+    if (wq::prefill_supported(a)) return wq::launch_prefill(a, s) == cudaSuccess ? WQ_OK : WQ_ERR_CUDA;
+  }
+  // Otherwise rows are processed 64 at a time (the decode kernel's token tile).
   for (int m0 = 0; m0 < M; m0 += 64) {
     a.M = (M - m0) < 64 ? (M - m0) : 64;
     a.x = static_cast<const uint16_t *>(x) + (size_t)m0 * K;

@@ -42,4 +42,12 @@ size_t decode_counter_bytes();
 DecodePlan plan_decode(int M, int N, int K, int w_bit, int group_size, bool zero, int sms);
 cudaError_t launch_decode(const MatmulArgs &a, const DecodePlan &p, void *workspace, cudaStream_t s);
 
+// Tensor-core path for many tokens (int4 codes, group size a multiple of 64,
+// scales in the x dtype).
+bool prefill_supported(const MatmulArgs &a);
+cudaError_t launch_prefill(const MatmulArgs &a, cudaStream_t s);
+
+// Token count from which wq_matmul takes the tensor-core path.
+constexpr int kPrefillMinM = 65;
+
 }  // namespace wq

@@ -1,0 +1,382 @@
+// prefill.cu -- weight-only quantized matmul for many tokens (tensor cores, tcgen05).
+//
+// At large M the step is bound by the multiply-adds, so the weights are
+// dequantized once per 128-token tile into shared memory in the operand
+// layout of the 5th-generation tensor cores, and tcgen05.mma accumulates
+// y^T-free:  D[m, n] (TMEM, fp32) += x[m, k] * w[k, n]  over 64-wide K steps.
+//
+// CTA tile: 128 tokens (UMMA M) x 256 output channels (UMMA N), K step 64.
+// Roles (10 warps):
+//   warp 0      producer: per stage one TMA copy of the x tile (128 x 64,
+//               128-byte swizzle), one 1-D bulk copy of the packed weights
+//               (256 channels x 64 k), and TMA copies of the scale and zero
+//               rows of the stage's group;
+//   warp 1      TMEM allocation and the single thread that issues tcgen05.mma;
+//   warps 2..9  dequant: w = (q - zero) * scale rounded once to the x dtype,
+//               written K-major with the 128-byte swizzle the MMA reads;
+//   warps 4..7  (after the main loop) epilogue: tcgen05.ld of the fp32
+//               accumulator, one token row per thread, stored to y.
+// The scale and zero are applied to the weight (one rounding to bf16/fp16),
+// since a per-group rescale of a 128 x 256 TMEM accumulator would cost more
+// than the tensor cores gain.
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "dev.cuh"
+#include "kernels.h"
+#include "layout.cuh"
+
+namespace wq {
+
+namespace pf {
+
+constexpr int BM = 128;   // tokens per CTA (UMMA M)
+constexpr int BN = 256;   // output channels per CTA (UMMA N)
+constexpr int BK = 64;    // K per stage: one 128-byte swizzle atom of bf16
+constexpr int STAGES = 4;
+constexpr int BSTAGES = 2;            // dequantized B buffers
+constexpr int DQ_WARPS = 8;
+constexpr int THREADS = (2 + DQ_WARPS) * 32;
+constexpr int A_BYTES = BM * BK * 2;  // 16 KB
+constexpr int B_BYTES = BN * BK * 2;  // 32 KB
+constexpr int W_BYTES = BN * BK / 2;  // 8 KB of packed int4
+constexpr int S_BYTES = BN * 2;       // one scale row
+constexpr int Z_BYTES = BN * 4;       // one zero-word row
+// stage = A | W | S | Z, 1024-byte aligned (the swizzle atom of A)
+constexpr int ST_A = 0, ST_W = A_BYTES, ST_S = ST_W + W_BYTES, ST_Z = ST_S + S_BYTES;
+constexpr int STAGE_BYTES = (ST_Z + Z_BYTES + 1023) / 1024 * 1024;
+constexpr int HEADER = 1024;          // mbarriers + TMEM address
+constexpr int SMEM = HEADER + STAGES * STAGE_BYTES + BSTAGES * B_BYTES;
+constexpr int TMEM_COLS = 256;
+
+struct Params {
+  CUtensorMap tm_x;  // x (M, K) 16-bit, box (64, 128), 128-byte swizzle
+  CUtensorMap tm_s;  // scales (G, N) 16-bit, box (256, 1)
+  CUtensorMap tm_z;  // zeros (ceil(G/8), N) 32-bit, box (256, 1)
+  const uint8_t *packed;
+  float *out;
+  uint32_t *err;
+  int M, N, K, gs, nt_total;
+};
+
+// Shared-memory matrix descriptor of a K-major operand with the 128-byte
+// swizzle: rows of 128 bytes, 8-row atoms 1024 bytes apart.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);  // start address
+  d |= (uint64_t)1 << 16;                     // leading byte offset (unused with this swizzle)
+  d |= (uint64_t)(1024 >> 4) << 32;           // stride byte offset: next 8-row atom
+  d |= (uint64_t)1 << 46;                     // descriptor version
+  d |= (uint64_t)2 << 61;                     // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor: fp32 accumulate, A and B both bf16 (or both fp16),
+// both K-major, M = 128, N = 256.
+template <bool BF16>
+__host__ __device__ constexpr uint32_t idesc() {
+  return (1u << 4) | ((BF16 ? 1u : 0u) << 7) | ((BF16 ? 1u : 0u) << 10) | ((uint32_t)(BN >> 3) << 17) |
+         ((uint32_t)(BM >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t id, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(id), "r"(acc)
+      : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Byte offset of element (row r, k) of a K-major 128-byte-swizzled bf16 tile.
+__device__ __forceinline__ uint32_t sw128_off(int r, int k) {
+  return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((((k * 2) >> 4) ^ (r & 7)) << 4) + ((k * 2) & 15));
+}
+
+__device__ __forceinline__ void sts64u(uint32_t a, uint32_t x, uint32_t y) {
+  asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(a), "r"(x), "r"(y) : "memory");
+}
+
+template <bool BF16>
+__device__ __forceinline__ uint32_t sub2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  if constexpr (BF16)
+    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  else
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+template <bool BF16>
+__device__ __forceinline__ uint32_t mul2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  if constexpr (BF16)
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  else
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// 32 consecutive fp32 columns of this warp's TMEM lane quarter.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%"
+      "28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+template <bool BF16, bool ZERO>
+__global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_constant__ Params p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // 1024-byte alignment (of the shared-window address) for the swizzled tiles
+  uint8_t *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem);          // TMA data of a stage landed
+  uint64_t *empty = full + STAGES;                                // MMA done with a stage
+  uint64_t *bfull = empty + STAGES;                               // dequantized B written
+  uint64_t *bempty = bfull + BSTAGES;                             // MMA done with a B buffer
+  uint64_t *accfull = bempty + BSTAGES;                           // accumulator complete
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(accfull + 1);
+  uint8_t *ring = smem + HEADER;
+  uint8_t *bbuf = ring + STAGES * STAGE_BYTES;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nb = blockIdx.x, mb = blockIdx.y;
+  const int n0 = nb * BN, m0 = mb * BM;
+  const int nt0 = n0 / 16;
+  const int ntiles = min(BN / 16, p.nt_total - nt0);
+  const int nk = p.K / BK;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < STAGES; ++i) {
+      mbar_init(smem_addr(&full[i]), 1);
+      mbar_init(smem_addr(&empty[i]), 1);
+    }
+    for (int i = 0; i < BSTAGES; ++i) {
+      mbar_init(smem_addr(&bfull[i]), DQ_WARPS);
+      mbar_init(smem_addr(&bempty[i]), 1);
+    }
+    mbar_init(smem_addr(accfull), 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(tmem_slot)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();
+      int issued = 0;
+      for (int i = 0; i < nk; ++i) {
+        const int st = i % STAGES;
+        if (i >= STAGES && !mbar_wait(smem_addr(&empty[st]), ((i / STAGES) - 1) & 1, p.err)) break;
+        const uint32_t fb = smem_addr(&full[st]);
+        const uint32_t base = smem_addr(ring + st * STAGE_BYTES);
+        const int g = i * BK / p.gs;
+        mbar_arrive_expect_tx(fb, A_BYTES + ntiles * 512 + S_BYTES + (ZERO ? Z_BYTES : 0));
+        tma_load_2d(base + ST_A, &p.tm_x, i * BK, m0, fb);
+        bulk_g2s(base + ST_W, p.packed + ((size_t)i * p.nt_total + nt0) * 512, ntiles * 512, fb, pol);
+        tma_load_2d(base + ST_S, &p.tm_s, n0, g, fb);
+        if (ZERO) tma_load_2d(base + ST_Z, &p.tm_z, n0, g / 8, fb);
+        issued = i + 1;
+      }
+      for (int i = max(0, issued - STAGES); i < issued; ++i)
+        mbar_wait(smem_addr(&full[i % STAGES]), (i / STAGES) & 1, p.err);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t id = idesc<BF16>();
+      for (int i = 0; i < nk; ++i) {
+        const int st = i % STAGES, sb = i % BSTAGES;
+        if (!mbar_wait(smem_addr(&full[st]), (i / STAGES) & 1, p.err)) break;
+        if (!mbar_wait(smem_addr(&bfull[sb]), (i / BSTAGES) & 1, p.err)) break;
+        tc_fence_after();
+        const uint32_t a0 = smem_addr(ring + st * STAGE_BYTES + ST_A);
+        const uint32_t b0 = smem_addr(bbuf + sb * B_BYTES);
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk)
+          umma(tmem, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), id, (i | kk) != 0);
+        umma_commit(smem_addr(&empty[st]));
+        umma_commit(smem_addr(&bempty[sb]));
+      }
+      umma_commit(smem_addr(accfull));  // every MMA issued above has completed when this fires
+    }
+  } else {
+    // ------------------------------------------------------------ dequant (warps 2..9)
+    const int dq = threadIdx.x - 64;  // 0 .. 255
+    constexpr uint32_t MAGIC = Magic<BF16>::kPair;
+    for (int i = 0; i < nk; ++i) {
+      const int st = i % STAGES, sb = i % BSTAGES;
+      if (!mbar_wait(smem_addr(&full[st]), (i / STAGES) & 1, p.err)) break;
+      if (i >= BSTAGES && !mbar_wait(smem_addr(&bempty[sb]), ((i / BSTAGES) - 1) & 1, p.err)) break;
+      const uint32_t base = smem_addr(ring + st * STAGE_BYTES);
+      const uint32_t bdst = smem_addr(bbuf + sb * B_BYTES);
+      const int g = i * BK / p.gs;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const int pr = dq + half * 256;  // (tile, lane) pair 0..511
+        const int tile = pr >> 5, ln = pr & 31;
+        if (tile < ntiles) {
+          const uint4 wv = lds128(base + ST_W + tile * 512 + ln * 16);
+          const int gq = ln >> 2, tq = ln & 3;
+          const uint32_t w4[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+          for (int r = 0; r < 2; ++r) {
+            const int col = tile * 16 + gq + 8 * r;  // row of B (output channel within the tile)
+            const uint16_t sbits = lds16(base + ST_S + col * 2);
+            uint32_t z = 8;
+            if (ZERO) z = (lds32(base + ST_Z + col * 4) >> ((g % 8) * 4)) & 15u;
+            const uint32_t zz = ((MAGIC & 0xFFFFu) + z) * 0x00010001u;  // (MAGIC + z) in both halves
+            const uint32_t ss = (uint32_t)sbits * 0x00010001u;
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const uint32_t w = w4[2 * u + r];
+#pragma unroll
+              for (int j = 0; j < 2; ++j) {
+                const uint32_t lo = mul2<BF16>(sub2<BF16>(code_pair<4, BF16>(w, 2 * j), zz), ss);
+                const uint32_t hi = mul2<BF16>(sub2<BF16>(code_pair<4, BF16>(w, 2 * j + 1), zz), ss);
+                const int k = 32 * u + 16 * j + 4 * tq;
+                sts64u(bdst + sw128_off(col, k), lo, hi);
+              }
+            }
+          }
+        }
+      }
+      fence_proxy_async_smem();  // generic-proxy writes -> visible to the tensor core
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&bfull[sb]));
+    }
+    // ---------------------------------------------------------- epilogue (warps 4..7)
+    if (warp >= 4 && warp < 8) {
+      const int q = warp & 3;  // TMEM lane quarter this warp may access
+      mbar_wait(smem_addr(accfull), 0, p.err);
+      tc_fence_after();
+      const int m = m0 + q * 32 + lane;
+      for (int c = 0; c < BN; c += 32) {
+        float v[32];
+        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + c, v);
+        if (m < p.M) {
+          float *dst = p.out + (size_t)m * p.N + n0 + c;
+          if (n0 + c + 32 <= p.N) {
+#pragma unroll
+            for (int j = 0; j < 32; j += 4)
+              *reinterpret_cast<float4 *>(dst + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (n0 + c + j < p.N) dst[j] = v[j];
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
+  }
+}
+
+}  // namespace pf
+
+// ------------------------------------------------------------------ host side
+typedef CUresult (*EncodeTiledFn2)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn2 encode_fn2() {
+  static EncodeTiledFn2 fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    void *f = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn2>(f);
+    tried = true;
+  }
+  return fn;
+}
+
+static bool enc(CUtensorMap *m, const void *base, int esize, uint64_t cols, uint64_t rows, uint32_t bc, uint32_t br,
+                CUtensorMapSwizzle sw) {
+  EncodeTiledFn2 fn = encode_fn2();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * (uint64_t)esize};
+  const cuuint32_t box[2] = {bc, br};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, esize == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void *>(base),
+            dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool prefill_supported(const MatmulArgs &a) {
+  return a.w_bit == 4 && a.group_size % pf::BK == 0 && a.K % pf::BK == 0 && a.x_bf16 == a.s_bf16;
+}
+
+template <bool BF16, bool ZERO>
+static cudaError_t launch_t(const pf::Params &pp, dim3 grid, cudaStream_t s) {
+  auto kern = pf::prefill_kernel<BF16, ZERO>;
+  static int attr_set[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const int smem = pf::SMEM + 1024;  // + slack for the 1024-byte alignment of the ring
+  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = 1;
+  }
+  kern<<<grid, pf::THREADS, smem, s>>>(pp);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prefill(const MatmulArgs &a, cudaStream_t s) {
+  pf::Params pp{};
+  const int G = a.K / a.group_size;
+  if (!enc(&pp.tm_x, a.x, 2, (uint64_t)a.K, (uint64_t)a.M, pf::BK, pf::BM, CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  if (!enc(&pp.tm_s, a.scales, 2, (uint64_t)a.N, (uint64_t)G, pf::BN, 1, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return cudaErrorInvalidValue;
+  if (a.zeros &&
+      !enc(&pp.tm_z, a.zeros, 4, (uint64_t)a.N, (uint64_t)((G + 7) / 8), pf::BN, 1, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return cudaErrorInvalidValue;
+  pp.packed = static_cast<const uint8_t *>(a.packed);
+  pp.out = a.out;
+  pp.err = a.err;
+  pp.M = a.M;
+  pp.N = a.N;
+  pp.K = a.K;
+  pp.gs = a.group_size;
+  pp.nt_total = a.N / 16;
+  dim3 grid((a.N + pf::BN - 1) / pf::BN, (a.M + pf::BM - 1) / pf::BM);
+  const bool z = a.zeros != nullptr;
+  if (a.x_bf16) return z ? launch_t<true, true>(pp, grid, s) : launch_t<true, false>(pp, grid, s);
+  return z ? launch_t<false, true>(pp, grid, s) : launch_t<false, false>(pp, grid, s);
+}
+
+}  // namespace wq
