@@ -147,6 +147,32 @@ WQ_API wq_status wq_matmul(const void *x, wq_dtype x_dtype, const void *packed_w
                     float *out, void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * wq_matmul_noalloc -- wq_matmul for callers that cannot allocate device memory.
+ *
+ * The pages have no counterpart to this entry point.  It exists for callers
+ * that must not allocate at call time and cannot hand the library a
+ * workspace: for example a plugin inside a host framework that owns every
+ * device allocation, or a latency-critical path that cannot afford
+ * cudaMalloc (which may synchronise the device).
+ *
+ * Same arguments and result as wq_matmul, without the workspace.  Its scratch
+ * is a fixed 8 MiB array inside the library image that every GPU which loads
+ * the library keeps until the process exits; no call allocates or frees
+ * anything.  A problem whose wq_workspace_bytes() exceeds 8 MiB returns
+ * WQ_ERR_WORKSPACE (use wq_matmul with a workspace instead).
+ *  - The first call on a device (made with that device current) looks up the
+ *    array's device address; make that first call before any stream capture.
+ *  - All calls share the one array and it keeps the previous call's
+ *    contents; each call clears the part that must start at zero.  Calls whose
+ *    kernels overlap on the GPU (different streams, or different host
+ *    threads) race on the array: serialise them.
+ */
+WQ_API wq_status wq_matmul_noalloc(const void *x, wq_dtype x_dtype, const void *packed_w,
+                                   const void *scales, wq_dtype s_dtype, const int32_t *zeros,
+                                   int M, int N, int K, int w_bit, int group_size,
+                                   float *out, void *stream);
+
+/*
  * wq_check_device -- synchronise `stream`, then read and clear the device
  * word in which kernels record a barrier wait that gave up.  Returns
  * WQ_ERR_TIMEOUT if one did, WQ_ERR_CUDA on a runtime error, else WQ_OK.

@@ -21,7 +21,7 @@ STATUS = ["WQ_OK", "WQ_ERR_NULL", "WQ_ERR_SHAPE", "WQ_ERR_WBIT", "WQ_ERR_GROUP",
           "WQ_ERR_ALIGN", "WQ_ERR_WORKSPACE", "WQ_ERR_ARCH", "WQ_ERR_CUDA", "WQ_ERR_TIMEOUT"]
 
 EXPORTS = ("wq_status_string", "wq_chunk_k", "wq_packed_bytes", "wq_pack", "wq_unpack",
-           "wq_workspace_bytes", "wq_matmul", "wq_check_device")
+           "wq_workspace_bytes", "wq_matmul", "wq_matmul_noalloc", "wq_check_device")
 
 
 class WQError(RuntimeError):
@@ -56,6 +56,8 @@ def lib() -> ctypes.CDLL:
         L.wq_workspace_bytes.argtypes = [I, I, I, I, I]
         L.wq_matmul.restype = I
         L.wq_matmul.argtypes = [P, I, P, P, I, P, I, I, I, I, I, P, P, Z, P]
+        L.wq_matmul_noalloc.restype = I
+        L.wq_matmul_noalloc.argtypes = [P, I, P, P, I, P, I, I, I, I, I, P, P]
         L.wq_check_device.restype = I
         L.wq_check_device.argtypes = [P]
         _lib = L
@@ -142,6 +144,20 @@ def wq_matmul(x: torch.Tensor, packed_w: torch.Tensor, scales: torch.Tensor, zer
                          _DTYPE.get(scales.dtype, -1), _ptr(zeros), M, N, K, w_bit, group_size,
                          _ptr(out), _ptr(workspace), ws_bytes, _stream(stream))
     _check(st, "wq_matmul")
+    return out
+
+
+def wq_matmul_noalloc(x: torch.Tensor, packed_w: torch.Tensor, scales: torch.Tensor,
+                      zeros: torch.Tensor | None, M: int, N: int, K: int, w_bit: int, group_size: int,
+                      out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Same as wq_matmul, through the C entry point that uses the library's own
+    fixed scratch instead of a caller workspace (no allocation on any call)."""
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    st = lib().wq_matmul_noalloc(_ptr(x), _DTYPE.get(x.dtype, -1), _ptr(packed_w), _ptr(scales),
+                                 _DTYPE.get(scales.dtype, -1), _ptr(zeros), M, N, K, w_bit, group_size,
+                                 _ptr(out), _stream(stream))
+    _check(st, "wq_matmul_noalloc")
     return out
 
 
