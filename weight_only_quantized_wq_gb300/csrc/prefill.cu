@@ -1,13 +1,15 @@
 // prefill.cu -- weight-only quantized matmul for many tokens (tensor cores, tcgen05).
 //
 // At large M the step is bound by the multiply-adds, so the weights are
-// dequantized once per 128-token tile into shared memory in the operand
+// dequantized once per 256-token tile into shared memory in the operand
 // layout of the 5th-generation tensor cores, and tcgen05.mma accumulates
 // y^T-free:  D[m, n] (TMEM, fp32) += x[m, k] * w[k, n]  over 64-wide K steps.
 //
-// CTA tile: 128 tokens (UMMA M) x 256 output channels (UMMA N), K step 64.
+// CTA tile: 256 tokens x 256 output channels, K step 64: two 128 x 256
+// accumulators (the whole 512-column TMEM) share each dequantized weight
+// tile, so every weight is dequantized once per 256 tokens.
 // Roles (10 warps):
-//   warp 0      producer: per stage one TMA copy of the x tile (128 x 64,
+//   warp 0      producer: per stage one TMA copy of the x tile (256 x 64,
 //               128-byte swizzle), one 1-D bulk copy of the packed weights
 //               (256 channels x 64 k), and TMA copies of the scale and zero
 //               rows of the stage's group;
@@ -31,14 +33,16 @@ namespace wq {
 
 namespace pf {
 
-constexpr int BM = 128;   // tokens per CTA (UMMA M)
+constexpr int UM = 128;   // UMMA M (tokens per accumulator)
+constexpr int MSUB = 2;   // accumulators per CTA
+constexpr int BM = UM * MSUB;  // tokens per CTA
 constexpr int BN = 256;   // output channels per CTA (UMMA N)
 constexpr int BK = 64;    // K per stage: one 128-byte swizzle atom of bf16
-constexpr int STAGES = 4;
+constexpr int STAGES = 3;
 constexpr int BSTAGES = 2;            // dequantized B buffers
 constexpr int DQ_WARPS = 8;
 constexpr int THREADS = (2 + DQ_WARPS) * 32;
-constexpr int A_BYTES = BM * BK * 2;  // 16 KB
+constexpr int A_BYTES = BM * BK * 2;  // 32 KB
 constexpr int B_BYTES = BN * BK * 2;  // 32 KB
 constexpr int W_BYTES = BN * BK / 2;  // 8 KB of packed int4
 constexpr int S_BYTES = BN * 2;       // one scale row
@@ -48,10 +52,10 @@ constexpr int ST_A = 0, ST_W = A_BYTES, ST_S = ST_W + W_BYTES, ST_Z = ST_S + S_B
 constexpr int STAGE_BYTES = (ST_Z + Z_BYTES + 1023) / 1024 * 1024;
 constexpr int HEADER = 1024;          // mbarriers + TMEM address
 constexpr int SMEM = HEADER + STAGES * STAGE_BYTES + BSTAGES * B_BYTES;
-constexpr int TMEM_COLS = 256;
+constexpr int TMEM_COLS = BN * MSUB;  // 512
 
 struct Params {
-  CUtensorMap tm_x;  // x (M, K) 16-bit, box (64, 128), 128-byte swizzle
+  CUtensorMap tm_x;  // x (M, K) 16-bit, box (64, 256), 128-byte swizzle
   CUtensorMap tm_s;  // scales (G, N) 16-bit, box (256, 1)
   CUtensorMap tm_z;  // zeros (ceil(G/8), N) 32-bit, box (256, 1)
   const uint8_t *packed;
@@ -77,7 +81,7 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
 template <bool BF16>
 __host__ __device__ constexpr uint32_t idesc() {
   return (1u << 4) | ((BF16 ? 1u : 0u) << 7) | ((BF16 ? 1u : 0u) << 10) | ((uint32_t)(BN >> 3) << 17) |
-         ((uint32_t)(BM >> 4) << 24);
+         ((uint32_t)(UM >> 4) << 24);
 }
 
 __device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t id, uint32_t acc) {
@@ -217,8 +221,11 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
         const uint32_t a0 = smem_addr(ring + st * STAGE_BYTES + ST_A);
         const uint32_t b0 = smem_addr(bbuf + sb * B_BYTES);
 #pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk)
-          umma(tmem, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), id, (i | kk) != 0);
+        for (int h = 0; h < MSUB; ++h)
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk)
+            umma(tmem + h * BN, sw128_desc(a0 + h * (UM * 128) + kk * 32), sw128_desc(b0 + kk * 32), id,
+                 (i | kk) != 0);
         umma_commit(smem_addr(&empty[st]));
         umma_commit(smem_addr(&bempty[sb]));
       }
@@ -274,20 +281,22 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
       const int q = warp & 3;  // TMEM lane quarter this warp may access
       mbar_wait(smem_addr(accfull), 0, p.err);
       tc_fence_after();
-      const int m = m0 + q * 32 + lane;
-      for (int c = 0; c < BN; c += 32) {
-        float v[32];
-        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + c, v);
-        if (m < p.M) {
-          float *dst = p.out + (size_t)m * p.N + n0 + c;
-          if (n0 + c + 32 <= p.N) {
+      for (int h = 0; h < MSUB; ++h) {
+        const int m = m0 + h * UM + q * 32 + lane;
+        for (int c = 0; c < BN; c += 32) {
+          float v[32];
+          tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + h * BN + c, v);
+          if (m < p.M) {
+            float *dst = p.out + (size_t)m * p.N + n0 + c;
+            if (n0 + c + 32 <= p.N) {
 #pragma unroll
-            for (int j = 0; j < 32; j += 4)
-              *reinterpret_cast<float4 *>(dst + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
-          } else {
+              for (int j = 0; j < 32; j += 4)
+                *reinterpret_cast<float4 *>(dst + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+            } else {
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (n0 + c + j < p.N) dst[j] = v[j];
+              for (int j = 0; j < 32; ++j)
+                if (n0 + c + j < p.N) dst[j] = v[j];
+            }
           }
         }
       }
