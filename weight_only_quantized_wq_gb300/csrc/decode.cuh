@@ -123,6 +123,7 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_min_blocks(MT, TN))
 
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ int s_last;
+  __shared__ volatile int s_abort;
   uint64_t *full = reinterpret_cast<uint64_t *>(smem);
   uint64_t *empty = full + STAGES;
   uint64_t *ready = empty + STAGES;
@@ -145,9 +146,11 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_min_blocks(MT, TN))
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
       mbar_init(smem_addr(&full[i]), 1);
-      mbar_init(smem_addr(&empty[i]), NW);
+      // a stage is free again once the consumers and (grouped codes) the prep warp are done with it
+      mbar_init(smem_addr(&empty[i]), GROUPED ? NW + 1 : NW);
       mbar_init(smem_addr(&ready[i]), 1);
     }
+    s_abort = 0;
     fence_barrier_init();
   }
   __syncthreads();
@@ -161,7 +164,7 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_min_blocks(MT, TN))
     if (lane == 0) {
       for (int i = 0; i < nch; ++i) {
         const int st = i % STAGES;
-        if (i >= STAGES && !mbar_wait(smem_addr(&empty[st]), ((i / STAGES) - 1) & 1, p.err)) break;
+        if (i >= STAGES && !mbar_wait(smem_addr(&empty[st]), ((i / STAGES) - 1) & 1, p.err, &s_abort)) break;
         const uint32_t fb = smem_addr(&full[st]);
         const uint32_t base = smem_addr(ring + st * SB);
         const int kc = c0 + i;
@@ -179,7 +182,7 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_min_blocks(MT, TN))
     // No copy may still be writing this CTA's shared memory when it exits.
     if (lane == 0)
       for (int i = max(0, issued - STAGES); i < issued; ++i)
-        mbar_wait(smem_addr(&full[i % STAGES]), (i / STAGES) & 1, p.err);
+        mbar_wait(smem_addr(&full[i % STAGES]), (i / STAGES) & 1, p.err, nullptr);
     return;
   }
 
@@ -192,7 +195,7 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_min_blocks(MT, TN))
       for (int i = 0; i < nch; ++i) {
         const int st = i % STAGES;
         bool ok = true;
-        if (lane == 0) ok = mbar_wait(smem_addr(&full[st]), (i / STAGES) & 1, p.err);
+        if (lane == 0) ok = mbar_wait(smem_addr(&full[st]), (i / STAGES) & 1, p.err, &s_abort);
         if (!__shfl_sync(0xffffffffu, ok, 0)) break;
         const uint32_t base = smem_addr(ring + st * SB);
         const int kc = c0 + i;
@@ -214,7 +217,10 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_min_blocks(MT, TN))
           }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_addr(&ready[st]));
+        if (lane == 0) {
+          mbar_arrive(smem_addr(&ready[st]));
+          mbar_arrive(smem_addr(&empty[st]));  // done reading this stage's scale / zero rows
+        }
       }
     }
     return;
@@ -241,9 +247,17 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_min_blocks(MT, TN))
   int gi = GROUPED ? kstep0 / p.kspg : 0;               // current group
   int kleft = GROUPED ? p.kspg - kstep0 % p.kspg : 0;  // k-steps left in it
 
+  // A barrier test returns after a long latency even when the phase is
+  // complete, so a non-blocking test of each stage's barrier is issued one
+  // stage early and its answer is only read when that stage starts.
+  bool next_ready = nch > 0 && mbar_test_wait(smem_addr(&full[0]), 0);
   for (int i = 0; i < nch; ++i) {
     const int st = i % STAGES;
-    if (!mbar_wait(smem_addr(GROUPED ? &ready[st] : &full[st]), (i / STAGES) & 1, p.err)) break;
+    // The weights and x are ready when the copies land; the prep warp's (s, z)
+    // pairs are only needed at a group's end, so that wait comes later.
+    if (!next_ready && !mbar_wait(smem_addr(&full[st]), (i / STAGES) & 1, p.err, &s_abort)) break;
+    if (i + 1 < nch) next_ready = mbar_test_wait(smem_addr(&full[(i + 1) % STAGES]), ((i + 1) / STAGES) & 1);
+    const int gi_stage = gi;  // group of this stage's first k: the stage's group row 0
     const uint32_t base = smem_addr(ring + st * SB);
     uint4 wv[TN];
 #pragma unroll
@@ -290,7 +304,8 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_min_blocks(MT, TN))
       }
       if (GROUPED && (--kleft == 0 || i * G::KS + ks + 1 == ksteps)) {
         // Group done: fold P and X of this group into the output accumulators.
-        const int r = gi - (c0 + i) * G::KC / p.gs;  // group row inside this stage
+        mbar_wait(smem_addr(&ready[st]), (i / STAGES) & 1, p.err, &s_abort);
+        const int r = gi - gi_stage;  // group row inside this stage
         const uint32_t prow = base + poff + r * L::kPRow;
 #pragma unroll
         for (int ti = 0; ti < TN; ++ti)
@@ -347,13 +362,34 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_min_blocks(MT, TN))
   consumer_sync();
   if (!s_last) return;
   __threadfence();
-  const int rows = ntiles * 16;
-  for (int idx = threadIdx.x; idx < p.M * rows; idx += NW * 32) {
-    const int m = idx / rows, n = n0 + idx % rows;
-    float v = 0.f;
-    for (int sp = 0; sp < p.splits; ++sp) v += __ldcg(p.partial + ((size_t)sp * p.M + m) * p.N + n);
-    if (W == 8) v *= __ldg(sc32 + n);
-    p.out[(size_t)m * p.N + n] = v;
+  // Four consecutive columns per thread, every split's partial loaded before any add.
+  const int quads = ntiles * 4;  // rows of 16 columns -> 4 float4 each
+  for (int idx = threadIdx.x; idx < p.M * quads; idx += NW * 32) {
+    const int m = idx / quads, n = n0 + (idx % quads) * 4;
+    float4 part[8];
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int sp0 = 0; sp0 < p.splits; sp0 += 8) {
+      const int cnt = min(8, p.splits - sp0);
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (u < cnt) part[u] = __ldcg(reinterpret_cast<const float4 *>(p.partial + ((size_t)(sp0 + u) * p.M + m) * p.N + n));
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (u < cnt) {
+          v.x += part[u].x;
+          v.y += part[u].y;
+          v.z += part[u].z;
+          v.w += part[u].w;
+        }
+    }
+    if (W == 8) {
+      const float4 s4 = __ldg(reinterpret_cast<const float4 *>(sc32 + n));
+      v.x *= s4.x;
+      v.y *= s4.y;
+      v.z *= s4.z;
+      v.w *= s4.w;
+    }
+    *reinterpret_cast<float4 *>(p.out + (size_t)m * p.N + n) = v;
   }
   if (threadIdx.x == 0) p.counters[nb] = 0;
 }

@@ -60,16 +60,36 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking test of the same condition (try_wait may suspend the thread).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait for the phase of `bar` with the given parity to complete.  Gives up
-// after kWaitLimitNs, records kDevErrTimeout in *err and returns false.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t *err) {
+// after kWaitLimitNs, records kDevErrTimeout in *err, raises the CTA's abort
+// flag and returns false.  When `abort` is given, a raised flag (another
+// thread of the CTA gave up) also ends the wait at once; waits that must see
+// their copies land before the CTA exits pass nullptr.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t *err, volatile int *abort) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 255u) == 0u && global_timer_ns() - t0 > kWaitLimitNs) {
-      atomicOr(err, kDevErrTimeout);
-      return false;
+    if ((it & 255u) == 0u) {
+      if (abort && *abort) return false;
+      if (global_timer_ns() - t0 > kWaitLimitNs) {
+        atomicOr(err, kDevErrTimeout);
+        if (abort) *abort = 1;
+        return false;
+      }
     }
   }
 }

@@ -155,6 +155,7 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
   uint64_t *bempty = bfull + BSTAGES;                             // MMA done with a B buffer
   uint64_t *accfull = bempty + BSTAGES;                           // accumulator complete
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(accfull + 1);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
   uint8_t *ring = smem + HEADER;
   uint8_t *bbuf = ring + STAGES * STAGE_BYTES;
 
@@ -175,6 +176,7 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
       mbar_init(smem_addr(&bempty[i]), 1);
     }
     mbar_init(smem_addr(accfull), 1);
+    *abort_flag = 0;
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -195,7 +197,7 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
       int issued = 0;
       for (int i = 0; i < nk; ++i) {
         const int st = i % STAGES;
-        if (i >= STAGES && !mbar_wait(smem_addr(&empty[st]), ((i / STAGES) - 1) & 1, p.err)) break;
+        if (i >= STAGES && !mbar_wait(smem_addr(&empty[st]), ((i / STAGES) - 1) & 1, p.err, abort_flag)) break;
         const uint32_t fb = smem_addr(&full[st]);
         const uint32_t base = smem_addr(ring + st * STAGE_BYTES);
         const int g = i * BK / p.gs;
@@ -207,7 +209,7 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
         issued = i + 1;
       }
       for (int i = max(0, issued - STAGES); i < issued; ++i)
-        mbar_wait(smem_addr(&full[i % STAGES]), (i / STAGES) & 1, p.err);
+        mbar_wait(smem_addr(&full[i % STAGES]), (i / STAGES) & 1, p.err, nullptr);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -215,8 +217,8 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
       constexpr uint32_t id = idesc<BF16>();
       for (int i = 0; i < nk; ++i) {
         const int st = i % STAGES, sb = i % BSTAGES;
-        if (!mbar_wait(smem_addr(&full[st]), (i / STAGES) & 1, p.err)) break;
-        if (!mbar_wait(smem_addr(&bfull[sb]), (i / BSTAGES) & 1, p.err)) break;
+        if (!mbar_wait(smem_addr(&full[st]), (i / STAGES) & 1, p.err, abort_flag)) break;
+        if (!mbar_wait(smem_addr(&bfull[sb]), (i / BSTAGES) & 1, p.err, abort_flag)) break;
         tc_fence_after();
         const uint32_t a0 = smem_addr(ring + st * STAGE_BYTES + ST_A);
         const uint32_t b0 = smem_addr(bbuf + sb * B_BYTES);
@@ -237,8 +239,8 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
     constexpr uint32_t MAGIC = Magic<BF16>::kPair;
     for (int i = 0; i < nk; ++i) {
       const int st = i % STAGES, sb = i % BSTAGES;
-      if (!mbar_wait(smem_addr(&full[st]), (i / STAGES) & 1, p.err)) break;
-      if (i >= BSTAGES && !mbar_wait(smem_addr(&bempty[sb]), ((i / BSTAGES) - 1) & 1, p.err)) break;
+      if (!mbar_wait(smem_addr(&full[st]), (i / STAGES) & 1, p.err, abort_flag)) break;
+      if (i >= BSTAGES && !mbar_wait(smem_addr(&bempty[sb]), ((i / BSTAGES) - 1) & 1, p.err, abort_flag)) break;
       const uint32_t base = smem_addr(ring + st * STAGE_BYTES);
       const uint32_t bdst = smem_addr(bbuf + sb * B_BYTES);
       const int g = i * BK / p.gs;
@@ -279,7 +281,7 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
     // ---------------------------------------------------------- epilogue (warps 4..7)
     if (warp >= 4 && warp < 8) {
       const int q = warp & 3;  // TMEM lane quarter this warp may access
-      mbar_wait(smem_addr(accfull), 0, p.err);
+      mbar_wait(smem_addr(accfull), 0, p.err, nullptr);
       tc_fence_after();
       for (int h = 0; h < MSUB; ++h) {
         const int m = m0 + h * UM + q * 32 + lane;
