@@ -47,6 +47,8 @@ def parse_args():
     ap.add_argument("--m", type=int, default=16)
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--hold-s", type=float, default=0.6, help="seconds of identical launches before the timed region")
+    ap.add_argument("--kernel-only", action="store_true",
+                    help="only the timed kernel launches (no e2e, sweep, CPU baseline or clocks): for profilers")
     return ap.parse_args()
 
 
@@ -189,8 +191,20 @@ def time_graphs(p, sets, ws, steps, warmup, torch, wq, hold_s=0.0, dist=None):
     return e0.elapsed_time(e1) / 1e3
 
 
+def uses_prefill(p) -> bool:
+    """The library takes its tensor-core path for 65+ tokens of int4 codes whose
+    group size is a multiple of 64 and whose scales have the x dtype."""
+    return p.M >= 65 and p.w_bit == 4 and p.group_size % 64 == 0 and p.x_dtype == p.s_dtype
+
+
+def kernel_name(p) -> str:
+    if uses_prefill(p):
+        return "prefill_kernel (tcgen05)"
+    return "decode_kernel" if p.M <= 64 else "decode_kernel (64-row slices)"
+
+
 def launches_per_call(p) -> int:
-    return -(-p.M // 64)
+    return 1 if uses_prefill(p) else -(-p.M // 64)
 
 
 def time_e2e(p, sets, ws, steps, warmup, torch, wq):
@@ -239,7 +253,7 @@ def sweep(torch, wq, syn, l2, pk, src):
         sets, ws = make_sets(p, torch, wq, l2)
         n = 50 if p.M <= 256 else 10
         sec = time_graphs(p, sets, ws, n, 5, torch, wq) / n
-        e = {"workload": p.name, "M": p.M, "us": round(sec * 1e6, 2),
+        e = {"workload": p.name, "M": p.M, "kernel": kernel_name(p), "us": round(sec * 1e6, 2),
              "weight_GBps": round(p.weight_bytes() / sec / 1e9, 1),
              "total_GBps": round(p.total_bytes() / sec / 1e9, 1),
              "TFLOPs": round(p.flops / sec / 1e12, 2),
@@ -349,9 +363,11 @@ def main():
     p = get_problem(args)
     sets, ws = make_sets(p, torch, wq, l2)
     clocks = ClockSampler(local)
-    clocks.start()
-    sec = time_graphs(p, sets, ws, args.steps, args.warmup, torch, wq, hold_s=args.hold_s, dist=dist)
-    clk = clocks.stop()
+    if not args.kernel_only:
+        clocks.start()
+    sec = time_graphs(p, sets, ws, args.steps, args.warmup, torch, wq, hold_s=0 if args.kernel_only else args.hold_s,
+                      dist=dist)
+    clk = None if args.kernel_only else clocks.stop()
     if dist is not None:
         t = torch.tensor([sec], dtype=torch.float64, device="cuda")
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -362,10 +378,13 @@ def main():
     roof = roofline_entry(p, per_step, pk, pk_src)
     key = "%s|M=%d" % (args.workload, p.M)
     roof["traffic"] = traffic_for(key)
-    roof["kernel"] = "decode_kernel" if p.M <= 64 else "decode_kernel (64-row slices)"
+    roof["kernel"] = kernel_name(p)
     roof["launch_us"] = round(per_step / lpc * 1e6, 3)
 
-    e2e_sec, h2d, d2h = time_e2e(p, sets, ws, args.steps, args.warmup, torch, wq)
+    if args.kernel_only:
+        e2e_sec, h2d, d2h = sec, 0, 0
+    else:
+        e2e_sec, h2d, d2h = time_e2e(p, sets, ws, args.steps, args.warmup, torch, wq)
     e2e_val = world * p.weight_bytes() * args.steps / e2e_sec / 1e9
 
     line = {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -382,11 +401,12 @@ def main():
     if rank == 0:
         del sets
         torch.cuda.empty_cache()
-        if not args.no_sweep:
+        if not args.no_sweep and not args.kernel_only:
             line["sweep"] = sweep(torch, wq, syn, l2, pk, pk_src)
-        gbps, cores, sample, _ = cpu_measure(p, 1, 0)
-        line["cpu_baseline"] = {"value": round(gbps, 3), "unit": UNIT, "cores": cores, "kind": "oracle",
-                                "sample": sample}
+        if not args.kernel_only:
+            gbps, cores, sample, _ = cpu_measure(p, 1, 0)
+            line["cpu_baseline"] = {"value": round(gbps, 3), "unit": UNIT, "cores": cores, "kind": "oracle",
+                                    "sample": sample}
         print(json.dumps(line))
     if dist is not None:
         dist.barrier()
