@@ -160,7 +160,9 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
   uint8_t *bbuf = ring + STAGES * STAGE_BYTES;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nb = blockIdx.x, mb = blockIdx.y;
+  // Token tiles vary fastest across the grid, so the CTAs that read the same
+  // 256-channel weight block run at about the same time and share it in L2.
+  const int mb = blockIdx.x, nb = blockIdx.y;
   const int n0 = nb * BN, m0 = mb * BM;
   const int nt0 = n0 / 16;
   const int ntiles = min(BN / 16, p.nt_total - nt0);
@@ -384,7 +386,7 @@ cudaError_t launch_prefill(const MatmulArgs &a, cudaStream_t s) {
   pp.K = a.K;
   pp.gs = a.group_size;
   pp.nt_total = a.N / 16;
-  dim3 grid((a.N + pf::BN - 1) / pf::BN, (a.M + pf::BM - 1) / pf::BM);
+  dim3 grid((a.M + pf::BM - 1) / pf::BM, (a.N + pf::BN - 1) / pf::BN);
   const bool z = a.zeros != nullptr;
   if (a.x_bf16) return z ? launch_t<true, true>(pp, grid, s) : launch_t<true, false>(pp, grid, s);
   return z ? launch_t<false, true>(pp, grid, s) : launch_t<false, false>(pp, grid, s);
