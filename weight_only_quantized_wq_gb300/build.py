@@ -31,8 +31,27 @@ def nvcc() -> str:
     return p
 
 
+# decode_inst.cu is compiled once per (code width, group schedule) pair; the
+# dispatch in decode.cu lists the same pairs.
+DECODE_VARIANTS = [(2, 0), (2, 2), (2, 4), (2, -1), (4, 0), (4, 2), (4, -1), (8, 0)]
+
+
 def _sources():
     return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+
+
+def _units():
+    """(source, object name, extra flags) for every translation unit."""
+    units = []
+    for src in _sources():
+        base = os.path.basename(src)
+        if base == "decode_inst.cu":
+            for w, f in DECODE_VARIANTS:
+                tag = "w%d_f%s" % (w, "g" if f < 0 else f)
+                units.append((src, "decode_inst_%s.o" % tag, ["-DWQ_W=%d" % w, "-DWQ_FOLD=%d" % f]))
+        else:
+            units.append((src, base + ".o", []))
+    return units
 
 
 def _deps():
@@ -55,9 +74,10 @@ def build(force: bool = False, verbose: bool = False, extra: list[str] | None = 
     cc = nvcc()
     extra = extra or []
 
-    def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src) + ".o")
-        cmd = [cc, *ARCH, *FLAGS, *extra, "-c", src, "-o", obj]
+    def compile_one(unit):
+        src, name, defs = unit
+        obj = os.path.join(BUILD, name)
+        cmd = [cc, *ARCH, *FLAGS, *defs, *extra, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError("nvcc failed on %s:\n%s%s" % (src, r.stdout, r.stderr))
@@ -65,8 +85,8 @@ def build(force: bool = False, verbose: bool = False, extra: list[str] | None = 
             print(r.stdout + r.stderr)
         return obj
 
-    with cf.ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 4)) as ex:
-        objs = list(ex.map(compile_one, _sources()))
+    with cf.ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 4)) as ex:
+        objs = list(ex.map(compile_one, _units()))
     tmp = LIB + ".%d.tmp" % os.getpid()
     r = subprocess.run([cc, *ARCH, "-shared", "-o", tmp, *objs], capture_output=True, text=True)
     if r.returncode != 0:

@@ -67,6 +67,17 @@ wq_status check_kn(int K, int N, int w_bit) {
   return WQ_OK;
 }
 
+// Workspace of a call: the largest over its 64-row slices of the few-token
+// kernel (full slices and the remainder).
+size_t slice_workspace(int M, int N, int K, int w_bit, int group_size, bool zero, int sms) {
+  size_t ws = wq::plan_decode(M < 64 ? M : 64, N, K, w_bit, group_size, zero, sms).workspace;
+  if (M > 64 && M % 64 != 0) {
+    const size_t r = wq::plan_decode(M % 64, N, K, w_bit, group_size, zero, sms).workspace;
+    ws = r > ws ? r : ws;
+  }
+  return ws;
+}
+
 }  // namespace
 
 extern "C" {
@@ -123,8 +134,10 @@ size_t wq_workspace_bytes(int M, int N, int K, int w_bit, int group_size) {
   if (M <= 0 || check_kn(K, N, w_bit) != WQ_OK) return 0;
   DeviceInfo *d = nullptr;
   if (device_info(&d) != WQ_OK) return 0;
-  // The split (and so the workspace) does not depend on the zeros or the group size.
-  return wq::plan_decode(M, N, K, w_bit, group_size, true, d->sms).workspace;
+  if (w_bit == 8 || group_size == -1) group_size = K;
+  if (group_size <= 0 || K % group_size != 0) return 0;
+  // The split (and so the workspace) does not depend on the zeros.
+  return slice_workspace(M, N, K, w_bit, group_size, true, d->sms);
 }
 
 wq_status wq_matmul(const void *x, wq_dtype x_dtype, const void *packed_w, const void *scales, wq_dtype s_dtype,
@@ -150,9 +163,10 @@ wq_status wq_matmul(const void *x, wq_dtype x_dtype, const void *packed_w, const
   DeviceInfo *d = nullptr;
   if ((st = device_info(&d)) != WQ_OK) return st;
 
-  const wq::DecodePlan plan = wq::plan_decode(M, N, K, w_bit, group_size, zeros != nullptr, d->sms);
-  if (plan.workspace > 0) {
-    if (!workspace || workspace_bytes < plan.workspace) return WQ_ERR_WORKSPACE;
+  const bool zero = zeros != nullptr;
+  const size_t need = slice_workspace(M, N, K, w_bit, group_size, zero, d->sms);
+  if (need > 0) {
+    if (!workspace || workspace_bytes < need) return WQ_ERR_WORKSPACE;
     if (!aligned(workspace, 16)) return WQ_ERR_ALIGN;
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -173,13 +187,14 @@ wq_status wq_matmul(const void *x, wq_dtype x_dtype, const void *packed_w, const
     a.out = out;
     if (wq::prefill_supported(a)) return wq::launch_prefill(a, s) == cudaSuccess ? WQ_OK : WQ_ERR_CUDA;
   }
-  // Otherwise rows are processed 64 at a time (the decode kernel's token tile).
+  // Otherwise rows are processed 64 at a time (the few-token kernel's largest token tile).
+  const wq::DecodePlan full = wq::plan_decode(M < 64 ? M : 64, N, K, w_bit, group_size, zero, d->sms);
   for (int m0 = 0; m0 < M; m0 += 64) {
     a.M = (M - m0) < 64 ? (M - m0) : 64;
     a.x = static_cast<const uint16_t *>(x) + (size_t)m0 * K;
     a.out = out + (size_t)m0 * N;
     const wq::DecodePlan p =
-        (M <= 64 || a.M == 64) ? plan : wq::plan_decode(a.M, N, K, w_bit, group_size, zeros != nullptr, d->sms);
+        (a.M == (M < 64 ? M : 64)) ? full : wq::plan_decode(a.M, N, K, w_bit, group_size, zero, d->sms);
     if (wq::launch_decode(a, p, workspace, s) != cudaSuccess) return WQ_ERR_CUDA;
   }
   return WQ_OK;

@@ -25,19 +25,19 @@ static EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// Row-major 2-D tensor (rows x cols, `esize`-byte elements) and a box of
-// (box_cols x box_rows), no swizzle, zero fill outside the tensor.
-static bool encode_2d(CUtensorMap *m, const void *base, int esize, uint64_t cols, uint64_t rows, uint32_t box_cols,
+// Row-major 2-D 16-bit tensor (rows x cols) and a box of (box_cols x box_rows),
+// no swizzle, zero fill outside the tensor.
+static bool encode_2d(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows, uint32_t box_cols,
                       uint32_t box_rows) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[2] = {cols, rows};
-  const cuuint64_t strides[1] = {cols * (uint64_t)esize};
+  const cuuint64_t strides[1] = {cols * 2};
   const cuuint32_t box[2] = {box_cols, box_rows};
   const cuuint32_t estr[2] = {1, 1};
-  return fn(m, esize == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void *>(base),
-            dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // The workspace starts with a fixed region of kMaxColumnBlocks arrival
@@ -46,32 +46,31 @@ static bool encode_2d(CUtensorMap *m, const void *base, int esize, uint64_t cols
 // call has: a workspace left zeroed by one call is ready for any other.
 size_t decode_counter_bytes() { return (size_t)kMaxColumnBlocks * sizeof(int); }
 
-// Largest number of groups any chunk row of KC values touches.
-static int groups_per_chunk(int K, int kc, int gs) {
-  int best = 1;
-  for (int c = 0; c < K / kc; ++c) {
-    const int r = ((c + 1) * kc - 1) / gs - (c * kc) / gs + 1;
-    best = r > best ? r : best;
-  }
-  return best;
-}
-
-static int align128(int v) { return (v + 127) / 128 * 128; }
-
-static int x_pitch_for(int w_bit) {
-  const int words = (256 / w_bit) / 2;
-  return 4 * (words + ((8 - words % 32) + 32) % 32);
-}
-
-// Mirrors DecodeLayout<W, MT, TN>::stage_bytes.
-static int stage_bytes_for(int w_bit, int mt, int tn, int gcap, bool zero) {
+// Group schedule of the kernel instantiations (decode_inst.cu is compiled for
+// these values): int4 chunks span 64 k, int2 chunks 128 k, int8 chunks 32 k.
+static int fold_for(int w_bit, int gs) {
   const int kc = 256 / w_bit;
-  const int cols = kDecodeWarps * tn * 16;
-  const int soff = align128(cols * kc * w_bit / 8 + mt * 8 * x_pitch_for(w_bit));
-  if (w_bit == 8) return soff;
-  const int zoff = align128(soff + gcap * cols * 2);
-  const int poff = align128(zoff + (zero ? 2 * cols * 4 : 0));
-  return align128(poff + gcap * cols * 8);
+  if (w_bit == 8 || gs % kc == 0) return 0;
+  if (kc % gs == 0) {
+    const int f = gs / 16;
+    if (w_bit == 4 && f == 2) return 2;
+    if (w_bit == 2 && (f == 2 || f == 4)) return f;
+  }
+  return -1;
+}
+
+// Scale rows and zero-word rows one CTA's K range touches, for splits of cps chunk rows.
+static void rows_for(int K, int kc, int gs, int cps, int V, int *srows, int *zrows) {
+  int sr = 1, zr = 1;
+  const int kch = K / kc;
+  for (int c0 = 0; c0 < kch; c0 += cps) {
+    const int kb = c0 * kc, ke = (c0 + cps < kch ? c0 + cps : kch) * kc;
+    const int ga = kb / gs, gb = (ke - 1) / gs;
+    sr = gb - ga + 1 > sr ? gb - ga + 1 : sr;
+    zr = gb / V - ga / V + 1 > zr ? gb / V - ga / V + 1 : zr;
+  }
+  *srows = sr;
+  *zrows = zr;
 }
 
 DecodePlan plan_decode(int M, int N, int K, int w_bit, int group_size, bool zero, int sms) {
@@ -82,7 +81,8 @@ DecodePlan plan_decode(int M, int N, int K, int w_bit, int group_size, bool zero
   const int nt = N / 16;
   const int kch = K / kc;
   const int gs = (w_bit == 8 || group_size <= 0) ? K : group_size;
-  const int gcap = w_bit == 8 ? 0 : groups_per_chunk(K, kc, gs);
+  const bool grouped = w_bit != 8;
+  const int V = 32 / w_bit;
   int tns[2] = {4, 2};
   int ntn = 2;
   if (mt == 4) { tns[0] = 2; ntn = 1; }
@@ -91,24 +91,27 @@ DecodePlan plan_decode(int M, int N, int K, int w_bit, int group_size, bool zero
   for (int a = 0; a < ntn; ++a) {
     const int tn = tns[a];
     const int nblocks = (nt + kDecodeWarps * tn - 1) / (kDecodeWarps * tn);
-    const int smem = kDecodeHeader + decode_stages(tn) * stage_bytes_for(w_bit, mt, tn, gcap, zero);
-    int occ = decode_min_blocks(mt, tn);  // the register budget the kernel is compiled for
-    const int by_smem = (228 * 1024) / (smem + 1024);
-    occ = occ < by_smem ? occ : by_smem;
-    if (occ < 1) occ = 1;
-    const long slots = (long)sms * occ;
-    const int smax = kch < 64 ? kch : 64;
+    const int smax = kch < 256 ? kch : 256;
     for (int s = 1; s <= smax; ++s) {
       const int cps = (kch + s - 1) / s;
       const int sreal = (kch + cps - 1) / cps;
       if (s != sreal) continue;
+      int srows = 0, zrows = 0;
+      if (grouped) rows_for(K, kc, gs, cps, V, &srows, &zrows);
+      if (!zero) zrows = 0;
+      const int smem = DecodeSmem{w_bit, mt, tn, srows, zrows}.bytes();
+      if (smem > 200 * 1024) continue;
+      int occ = decode_min_blocks(mt, tn);  // the register budget the kernel is compiled for
+      const int by_smem = (228 * 1024) / (smem + 1024);
+      occ = occ < by_smem ? occ : by_smem;
+      if (occ < 1) continue;
+      const long slots = (long)sms * occ;
       const long units = (long)nblocks * sreal;
       // weight bytes the busiest SM streams (one wave if the units fit the slots)
       const long per_sm = units <= slots ? (units + sms - 1) / sms : ((units + slots - 1) / slots) * occ;
-      double cost = (double)per_sm * cps * tn * kDecodeWarps * 512.0;
+      double cost = (double)per_sm * (cps * (double)tn * kDecodeWarps * 512.0 + 8192.0);
       // the partial sums' round trip, spread over the SMs
       if (sreal > 1) cost += 8.0 * rows * (double)N * sreal / sms;
-      if (tn < 4) cost *= 1.05;  // narrower CTAs spend more instructions per weight on the activations
       if (cost < best_cost * 0.999) {
         best_cost = cost;
         best.mt = mt;
@@ -116,61 +119,53 @@ DecodePlan plan_decode(int M, int N, int K, int w_bit, int group_size, bool zero
         best.nblocks = nblocks;
         best.splits = sreal;
         best.cps = cps;
+        best.srows = srows;
+        best.zrows = zrows;
+        best.smem = smem;
       }
     }
   }
-  best.gcap = gcap;
-  best.stage_bytes = stage_bytes_for(w_bit, best.mt, best.tn, gcap, zero);
+  best.fold = fold_for(w_bit, gs);
   best.workspace = best.splits > 1 ? decode_counter_bytes() + (size_t)best.splits * rows * N * sizeof(float) : 0;
   return best;
 }
 
 cudaError_t launch_decode(const MatmulArgs &a, const DecodePlan &p, void *workspace, cudaStream_t s) {
   DecodeParams dp{};
-  dp.x = static_cast<const uint16_t *>(a.x);
   dp.packed = static_cast<const uint8_t *>(a.packed);
+  dp.err = a.err;
   dp.scales = a.scales;
   dp.zeros = a.zeros;
   dp.out = a.out;
-  dp.err = a.err;
   dp.M = a.M;
   dp.N = a.N;
   dp.K = a.K;
   dp.gs = a.group_size;
-  dp.kspg = a.group_size / 16;
   dp.nt_total = a.N / 16;
   dp.kch = a.K / (256 / a.w_bit);
   dp.splits = p.splits;
   dp.cps = p.cps;
-  dp.gcap = p.gcap;
-  dp.stage_bytes = p.stage_bytes;
+  dp.srows = p.srows;
+  dp.zrows = p.zrows;
   dp.s_bf16 = a.s_bf16;
   if (p.splits > 1) {
     dp.counters = static_cast<int *>(workspace);
     dp.partial = reinterpret_cast<float *>(static_cast<char *>(workspace) + decode_counter_bytes());
   }
-  // Tensor maps for the activation slice and the scale / zero rows of a stage.
-  const int kc = 256 / a.w_bit;
-  const int cols = kDecodeWarps * p.tn * 16;
-  if (!encode_2d(&dp.tm_x, a.x, 2, (uint64_t)a.K, (uint64_t)a.M, (uint32_t)(x_pitch_for(a.w_bit) / 2),
-                 (uint32_t)(p.mt * 8)))
+  // Tensor map of the activation slice of a stage (rows past M read as zeros).
+  if (!encode_2d(&dp.tm_x, a.x, (uint64_t)a.K, (uint64_t)a.M, (uint32_t)(x_pitch(a.w_bit) / 2), (uint32_t)(p.mt * 8)))
     return cudaErrorInvalidValue;
-  if (a.w_bit != 8) {
-    const int G = a.K / a.group_size;
-    if (!encode_2d(&dp.tm_s, a.scales, 2, (uint64_t)a.N, (uint64_t)G, (uint32_t)cols, (uint32_t)p.gcap))
-      return cudaErrorInvalidValue;
-    if (a.zeros) {
-      const int V = 32 / a.w_bit;
-      if (!encode_2d(&dp.tm_z, a.zeros, 4, (uint64_t)a.N, (uint64_t)((G + V - 1) / V), (uint32_t)cols, 2u))
-        return cudaErrorInvalidValue;
-    }
-  }
-  (void)kc;
   const bool z = a.zeros != nullptr;
-  switch (a.w_bit) {
-    case 2: return launch_decode_w<2>(dp, p, a.x_bf16, z, s);
-    case 4: return launch_decode_w<4>(dp, p, a.x_bf16, z, s);
-    case 8: return launch_decode_w<8>(dp, p, a.x_bf16, false, s);
+  const bool bf = a.x_bf16;
+  switch (a.w_bit * 16 + p.fold) {
+    case 2 * 16 + 0: return launch_decode_wf<2, 0>(dp, p, bf, z, s);
+    case 2 * 16 + 2: return launch_decode_wf<2, 2>(dp, p, bf, z, s);
+    case 2 * 16 + 4: return launch_decode_wf<2, 4>(dp, p, bf, z, s);
+    case 2 * 16 - 1: return launch_decode_wf<2, -1>(dp, p, bf, z, s);
+    case 4 * 16 + 0: return launch_decode_wf<4, 0>(dp, p, bf, z, s);
+    case 4 * 16 + 2: return launch_decode_wf<4, 2>(dp, p, bf, z, s);
+    case 4 * 16 - 1: return launch_decode_wf<4, -1>(dp, p, bf, z, s);
+    case 8 * 16 + 0: return launch_decode_wf<8, 0>(dp, p, bf, false, s);
   }
   return cudaErrorInvalidValue;
 }

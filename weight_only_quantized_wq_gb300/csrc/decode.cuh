@@ -2,30 +2,34 @@
 //
 // The step is bound by reading the packed weights (the tiny-llm int8_gemv
 // docstring makes the same point for small M), so each weight byte is read
-// from HBM once, through a shared-memory ring, and turned into tensor-core
-// operands in registers.
+// from HBM once, through a deep shared-memory ring, and turned into
+// tensor-core operands in registers.
+//
+// Roles (5 warps): one producer lane issues, per ring stage (one chunk row of
+// KC values of K), a 1-D bulk copy of the packed weights of the CTA's 16*4*TN
+// output channels and a 2-D tensor copy of the activation slice; four
+// consumer warps (TN tiles of 16 channels each) wait for a stage, compute it
+// and release it.  Nothing else couples the warps: the scale and zero rows of
+// all of the CTA's groups are staged in shared memory once, at the start, so
+// a finished group is folded without waiting for anyone.
 //
 // Swap-AB: the weight tile (16 output channels x 16 k) is the A operand of
 // mma.m16n8k16 and the tokens are its N = 8 columns, so the output channels
 // fill the MMA's M dimension however few tokens there are.
 //
-// Ring stage = one chunk row (KC values of K) for the CTA's 16*NW*TN output
-// channels: the packed weights (one 1-D bulk copy), the activation slice,
-// and the scale / zero rows of the groups the chunk touches (three 2-D tensor
-// copies through tensor maps).  One lane of the producer warp issues all four
-// copies of a stage.
-// A prep warp turns each stage's scale / zero rows into per-column pairs
-// (s, -s * (MAGIC + zero)) so that the consumer warps fold a finished group
-// into their accumulators with two FMAs per value.
+// Exact group arithmetic (W = 2, 4): one shift and one LOP3 per pair turn two
+// codes into MAGIC + q (exact in fp16 / bf16) and one subtraction of
+// MAGIC + zero gives q - zero, a small integer, exactly.  The MMA sums
+// x (q - zero) over one group in fp32 and the group's scale is applied to that
+// sum (one FMA per value): no weight is ever rounded.  int8 codes (W = 8) are
+// converted exactly and the per-channel scale is applied at the end (tiny-llm
+// int8_matmul docstring).
 //
-// Grouped codes (W = 2, 4) enter the MMA as MAGIC + q, exact in fp16/bf16.
-// Per group g and output column n the kernel accumulates in fp32
-//   P = sum_k x[m,k] (MAGIC + q[k,n])   (tensor cores)
-//   X = sum_k x[m,k]                    (tensor cores, A operand all ones)
-// and adds scale[g,n] * (P - (MAGIC + zero[g,n]) * X) = scale * sum_k x (q - zero)
-// to the output accumulator: scale and zero cost once per group, not per weight.
-// int8 codes (W = 8) are converted exactly and the per-channel scale is
-// applied at the end (tiny-llm int8_matmul docstring).
+// Group schedule (template FOLD): FOLD > 0 when the group size 16*FOLD divides
+// the chunk (a group can end only after every FOLD-th k-step); FOLD == 0 when
+// the chunk divides the group size (groups end on chunk boundaries); FOLD < 0
+// for any other multiple of 16.  A CTA's K range may end inside a group
+// (split-K); that partial group is folded at the range's end.
 //
 // Split-K: when the column blocks alone leave SMs idle, the K range is split;
 // each CTA writes its fp32 partial to the workspace and the last CTA to
@@ -43,97 +47,79 @@
 
 namespace wq {
 
-constexpr int kDecodeWarps = 4;   // consumer warps per CTA (plus a producer and a prep warp)
-constexpr int kDecodeThreads = (kDecodeWarps + 2) * 32;
+constexpr int kDecodeWarps = 4;  // consumer warps per CTA (plus one producer warp)
+constexpr int kDecodeThreads = (kDecodeWarps + 1) * 32;
+constexpr int kDecodeHeader = 256;  // mbarriers in front of the staged rows
 // Ring depth: about 40 KB of weights in flight per CTA.
 __host__ __device__ constexpr int decode_stages(int tn) { return tn >= 4 ? 5 : 8; }
-constexpr int kDecodeHeader = 256;  // mbarriers in front of the ring
-// Resident CTAs per SM the register budget is sized for: wide accumulator
-// sets (token tiles x weight tiles >= 8) get two CTAs per SM and no spills.
+// Resident CTAs per SM the register budget is sized for.
 __host__ __device__ constexpr int decode_min_blocks(int mt, int tn) { return mt * tn >= 8 ? 2 : 3; }
+
+__host__ __device__ constexpr int align128(int v) { return (v + 127) / 128 * 128; }
 
 // Row pitch of the activation slice in shared memory: the 32-bit word count
 // is 8 mod 32, which makes the 8-byte B-fragment loads of a warp conflict-free.
-template <int W>
-__host__ __device__ constexpr int x_pitch() {
-  return 4 * (Geo<W>::KC / 2 + ((8 - (Geo<W>::KC / 2) % 32) + 32) % 32);
-}
+__host__ __device__ constexpr int x_pitch(int w) { return 4 * ((128 / w) + ((8 - (128 / w) % 32) + 32) % 32); }
+
+// Shared-memory layout of one CTA: barriers | staged scale rows | staged
+// zero-word rows | ring of stages (packed weights, then the activation slice).
+struct DecodeSmem {
+  int w, mt, tn, srows, zrows;
+  __host__ __device__ constexpr int cols() const { return kDecodeWarps * tn * 16; }
+  __host__ __device__ constexpr int s_off() const { return kDecodeHeader; }
+  __host__ __device__ constexpr int z_off() const { return align128(s_off() + srows * cols() * 2); }
+  __host__ __device__ constexpr int ring_off() const { return align128(z_off() + zrows * cols() * 4); }
+  __host__ __device__ constexpr int w_bytes() const { return cols() * 32; }  // one chunk row of weights
+  __host__ __device__ constexpr int x_off() const { return w_bytes(); }
+  __host__ __device__ constexpr int x_bytes() const { return mt * 8 * x_pitch(w); }
+  __host__ __device__ constexpr int stage_bytes() const { return align128(x_off() + x_bytes()); }
+  __host__ __device__ constexpr int bytes() const { return ring_off() + decode_stages(tn) * stage_bytes(); }
+};
 
 struct DecodeParams {
   CUtensorMap tm_x;  // x (M, K) 16-bit; box (x_pitch/2, 8*MT): the row pitch padding is real data or zeros
-  CUtensorMap tm_s;  // scales (G, N) 16-bit; box (cols, gcap)
-  CUtensorMap tm_z;  // zeros (ceil(G/V), N) 32-bit; box (cols, 2)
-  const uint16_t *x;
   const uint8_t *packed;
-  const void *scales;
-  const uint32_t *zeros;
+  const void *scales;     // (G, N) 16-bit, or (N,) fp32 for int8
+  const uint32_t *zeros;  // (ceil(G / V), N) or nullptr
   float *out;
   float *partial;
   int *counters;
   uint32_t *err;
-  int M, N, K, gs, kspg, nt_total, kch, splits, cps, gcap, stage_bytes;
+  int M, N, K, gs, nt_total, kch, splits, cps, srows, zrows;
   bool s_bf16;
 };
-
-template <int W, int MT, int TN>
-struct DecodeLayout {
-  static constexpr int kCols = kDecodeWarps * TN * 16;  // output channels per CTA
-  static constexpr int kWBytes = kCols * Geo<W>::KC * W / 8;
-  static constexpr int kXBytes = MT * 8 * x_pitch<W>();
-  static constexpr int kXOff = kWBytes;
-  static constexpr int kSOff = (kXOff + kXBytes + 127) / 128 * 128;
-  // Stage = weights | x | scale rows (gcap) | two zero rows | per group row:
-  // (s, -s*(MAGIC+z)) for each column.
-  static constexpr int kPRow = kCols * 8;
-  static __host__ __device__ constexpr int z_off(int gcap) { return (kSOff + gcap * kCols * 2 + 127) / 128 * 128; }
-  static __host__ __device__ constexpr int p_off(int gcap, bool zero) {
-    return (z_off(gcap) + (zero ? 2 * kCols * 4 : 0) + 127) / 128 * 128;
-  }
-  static __host__ __device__ constexpr int stage_bytes(int gcap, bool grouped, bool zero) {
-    return grouped ? (p_off(gcap, zero) + gcap * kPRow + 127) / 128 * 128 : kSOff;
-  }
-  // Bytes the tensor copies of one stage deliver (besides the weights).
-  static __host__ __device__ constexpr int tma_bytes(int gcap, bool grouped, bool zero) {
-    return kXBytes + (grouped ? gcap * kCols * 2 + (zero ? 2 * kCols * 4 : 0) : 0);
-  }
-};
-
-__device__ __forceinline__ void sts64(uint32_t a, float x, float y) {
-  asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(a), "f"(x), "f"(y) : "memory");
-}
-__device__ __forceinline__ float2 lds64f(uint32_t a) {
-  float2 v;
-  asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(a));
-  return v;
-}
 
 __device__ __forceinline__ void consumer_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(kDecodeWarps * 32) : "memory");
 }
 
-template <int W, bool BF16, int MT, int TN, bool ZERO>
+__device__ __forceinline__ uint4 ldg_nc128(const void *p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
+
+template <int W, bool BF16, int MT, int TN, bool ZERO, int FOLD>
 __global__ void __launch_bounds__(kDecodeThreads, decode_min_blocks(MT, TN))
     decode_kernel(const __grid_constant__ DecodeParams p) {
   using G = Geo<W>;
-  using L = DecodeLayout<W, MT, TN>;
   constexpr int NW = kDecodeWarps, STAGES = decode_stages(TN);
-  constexpr int XP = x_pitch<W>();
+  constexpr int KS = G::KS, KC = G::KC, WK = G::WK, V = G::V;
+  constexpr int XP = x_pitch(W);
   constexpr bool GROUPED = (W != 8);
-  constexpr int COLS = L::kCols;
+  constexpr int CC = NW * TN * 16;  // output channels per CTA
 
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ int s_last;
   __shared__ volatile int s_abort;
+  const DecodeSmem L{W, MT, TN, p.srows, p.zrows};
   uint64_t *full = reinterpret_cast<uint64_t *>(smem);
   uint64_t *empty = full + STAGES;
-  uint64_t *ready = empty + STAGES;
-  uint8_t *ring = smem + kDecodeHeader;
-  static_assert(3 * STAGES * 8 <= kDecodeHeader, "barriers do not fit the header");
-  const int SB = p.stage_bytes;
-  const int zoff = L::z_off(p.gcap);
-  const int poff = L::p_off(p.gcap, ZERO);
-  (void)zoff;
-  (void)poff;
+  static_assert(2 * STAGES * 8 <= kDecodeHeader, "barriers do not fit the header");
+  const uint16_t *s_sm = reinterpret_cast<const uint16_t *>(smem + L.s_off());  // [srows][CC]
+  const uint32_t *z_sm = reinterpret_cast<const uint32_t *>(smem + L.z_off());  // [zrows][CC]
+  uint8_t *ring = smem + L.ring_off();
+  const int SB = L.stage_bytes();
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nb = blockIdx.x, split = blockIdx.y;
@@ -142,13 +128,12 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_min_blocks(MT, TN))
   const int n0 = nt0 * 16;
   const int c0 = split * p.cps;
   const int nch = min(p.kch, c0 + p.cps) - c0;
+  const int kbeg = c0 * KC, kend = kbeg + nch * KC;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
       mbar_init(smem_addr(&full[i]), 1);
-      // a stage is free again once the consumers and (grouped codes) the prep warp are done with it
-      mbar_init(smem_addr(&empty[i]), GROUPED ? NW + 1 : NW);
-      mbar_init(smem_addr(&ready[i]), 1);
+      mbar_init(smem_addr(&empty[i]), NW);
     }
     s_abort = 0;
     fence_barrier_init();
@@ -159,7 +144,7 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_min_blocks(MT, TN))
     // ------------------------------------------------------------ producer
     const uint64_t pol_w = policy_evict_first();
     const uint32_t wbytes = (uint32_t)ntiles * 512u;
-    const uint32_t tbytes = (uint32_t)L::tma_bytes(p.gcap, GROUPED, ZERO);
+    const uint32_t xbytes = (uint32_t)L.x_bytes();
     int issued = 0;
     if (lane == 0) {
       for (int i = 0; i < nch; ++i) {
@@ -168,73 +153,47 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_min_blocks(MT, TN))
         const uint32_t fb = smem_addr(&full[st]);
         const uint32_t base = smem_addr(ring + st * SB);
         const int kc = c0 + i;
-        mbar_arrive_expect_tx(fb, wbytes + tbytes);
+        mbar_arrive_expect_tx(fb, wbytes + xbytes);
         bulk_g2s(base, p.packed + ((size_t)kc * p.nt_total + nt0) * 512, wbytes, fb, pol_w);
-        tma_load_2d(base + L::kXOff, &p.tm_x, kc * G::KC, 0, fb);
-        if (GROUPED) {
-          const int g0 = kc * G::KC / p.gs;
-          tma_load_2d(base + L::kSOff, &p.tm_s, n0, g0, fb);
-          if (ZERO) tma_load_2d(base + zoff, &p.tm_z, n0, g0 / G::V, fb);
-        }
+        tma_load_2d(base + L.x_off(), &p.tm_x, kc * KC, 0, fb);
         issued = i + 1;
       }
-    }
-    // No copy may still be writing this CTA's shared memory when it exits.
-    if (lane == 0)
+      // No copy may still be writing this CTA's shared memory when it exits.
       for (int i = max(0, issued - STAGES); i < issued; ++i)
         mbar_wait(smem_addr(&full[i % STAGES]), (i / STAGES) & 1, p.err, nullptr);
-    return;
-  }
-
-  if (warp == NW + 1) {
-    // ------------------------------------------------------------ prep
-    // (s, -s * (MAGIC + zero)) for every column of each group that ends in
-    // this stage (or is cut off by the end of this CTA's K range).
-    if (GROUPED) {
-      const int cols = ntiles * 16;
-      for (int i = 0; i < nch; ++i) {
-        const int st = i % STAGES;
-        bool ok = true;
-        if (lane == 0) ok = mbar_wait(smem_addr(&full[st]), (i / STAGES) & 1, p.err, &s_abort);
-        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-        const uint32_t base = smem_addr(ring + st * SB);
-        const int kc = c0 + i;
-        const int g0 = kc * G::KC / p.gs;
-        const int kend = (kc + 1) * G::KC;  // first k past this stage
-        const int glast = (kend - 1) / p.gs;
-        for (int g = g0; g <= glast; ++g) {
-          if ((g + 1) * p.gs > kend && i != nch - 1) continue;  // group continues in the next stage
-          const int r = g - g0;
-          const uint32_t srow = base + L::kSOff + r * COLS * 2;
-          const uint32_t zrow = base + zoff + (g / G::V - g0 / G::V) * COLS * 4;
-          const uint32_t prow = base + poff + r * L::kPRow;
-          const int zshift = (g % G::V) * W;
-          for (int c = lane; c < cols; c += 32) {
-            const float sv = half_bits_to_float(lds16(srow + c * 2), p.s_bf16);
-            uint32_t z = 1u << (W - 1);
-            if (ZERO) z = (lds32(zrow + c * 4) >> zshift) & ((1u << W) - 1u);
-            sts64(prow + c * 8, sv, -sv * (Magic<BF16>::kValue + (float)z));
-          }
-        }
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(smem_addr(&ready[st]));
-          mbar_arrive(smem_addr(&empty[st]));  // done reading this stage's scale / zero rows
-        }
-      }
     }
     return;
   }
 
   // -------------------------------------------------------------- consumers
   const int g = lane >> 2, t = lane & 3;
+  const int wt0 = warp * TN;  // first tile of this warp within the CTA
+
+  // Scale and zero rows of the CTA's groups -> shared memory (16-byte loads),
+  // while the producer fills the ring.
+  const int g0 = GROUPED ? kbeg / p.gs : 0;
+  if constexpr (GROUPED) {
+    const int ng = (kend - 1) / p.gs - g0 + 1;
+    const int cols = ntiles * 16;
+    uint16_t *sw = reinterpret_cast<uint16_t *>(smem + L.s_off());
+    const uint16_t *sg = static_cast<const uint16_t *>(p.scales);
+    for (int idx = threadIdx.x; idx < ng * (cols / 8); idx += NW * 32) {
+      const int row = idx / (cols / 8), c = (idx % (cols / 8)) * 8;
+      *reinterpret_cast<uint4 *>(sw + row * CC + c) = ldg_nc128(sg + (size_t)(g0 + row) * p.N + n0 + c);
+    }
+    if constexpr (ZERO) {
+      uint32_t *zw = reinterpret_cast<uint32_t *>(smem + L.z_off());
+      const int nz = (kend - 1) / p.gs / V - g0 / V + 1;
+      for (int idx = threadIdx.x; idx < nz * (cols / 4); idx += NW * 32) {
+        const int row = idx / (cols / 4), c = (idx % (cols / 4)) * 4;
+        *reinterpret_cast<uint4 *>(zw + row * CC + c) = ldg_nc128(p.zeros + (size_t)(g0 / V + row) * p.N + n0 + c);
+      }
+    }
+    consumer_sync();
+  }
+
   float acc[TN][MT][4];
   float accg[TN][MT][4];
-  float xs[MT][4];
-#pragma unroll
-  for (int j = 0; j < MT; ++j)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) xs[j][e] = 0.f;
 #pragma unroll
   for (int i = 0; i < TN; ++i)
 #pragma unroll
@@ -242,42 +201,74 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_min_blocks(MT, TN))
 #pragma unroll
       for (int e = 0; e < 4; ++e) acc[i][j][e] = accg[i][j][e] = 0.f;
 
-  const int kstep0 = c0 * G::KS;
-  const int ksteps = nch * G::KS;
-  int gi = GROUPED ? kstep0 / p.kspg : 0;               // current group
-  int kleft = GROUPED ? p.kspg - kstep0 % p.kspg : 0;  // k-steps left in it
+  // (MAGIC + zero) of the current group for rows g and g + 8 of every tile
+  uint32_t zz[TN][2];
+  auto set_zeros = [&](int gi) {
+#pragma unroll
+    for (int ti = 0; ti < TN; ++ti)
+#pragma unroll
+      for (int rr = 0; rr < 2; ++rr) {
+        uint32_t z = 1u << (W - 1);
+        if constexpr (ZERO)
+          z = (z_sm[(gi / V - g0 / V) * CC + (wt0 + ti) * 16 + g + 8 * rr] >> ((gi % V) * W)) & ((1u << W) - 1u);
+        zz[ti][rr] = ((Magic<BF16>::kPair & 0xFFFFu) + z) * 0x00010001u;
+      }
+  };
+  // acc += scale[gi] * (sum over group gi); the group sum restarts.
+  auto fold = [&](int gi) {
+#pragma unroll
+    for (int ti = 0; ti < TN; ++ti)
+#pragma unroll
+      for (int rr = 0; rr < 2; ++rr) {
+        const float s = half_bits_to_float(s_sm[(gi - g0) * CC + (wt0 + ti) * 16 + g + 8 * rr], p.s_bf16);
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            acc[ti][mt][2 * rr + c] = fmaf(s, accg[ti][mt][2 * rr + c], acc[ti][mt][2 * rr + c]);
+            accg[ti][mt][2 * rr + c] = 0.f;
+          }
+      }
+  };
 
-  // A barrier test returns after a long latency even when the phase is
+  int cur_g = g0;
+  int next_fold = GROUPED ? min((g0 + 1) * p.gs, kend) : kend;
+  if constexpr (GROUPED) set_zeros(g0);
+
+  // A barrier test returns after some latency even when the phase is
   // complete, so a non-blocking test of each stage's barrier is issued one
   // stage early and its answer is only read when that stage starts.
   bool next_ready = nch > 0 && mbar_test_wait(smem_addr(&full[0]), 0);
   for (int i = 0; i < nch; ++i) {
     const int st = i % STAGES;
-    // The weights and x are ready when the copies land; the prep warp's (s, z)
-    // pairs are only needed at a group's end, so that wait comes later.
     if (!next_ready && !mbar_wait(smem_addr(&full[st]), (i / STAGES) & 1, p.err, &s_abort)) break;
     if (i + 1 < nch) next_ready = mbar_test_wait(smem_addr(&full[(i + 1) % STAGES]), ((i + 1) / STAGES) & 1);
-    const int gi_stage = gi;  // group of this stage's first k: the stage's group row 0
     const uint32_t base = smem_addr(ring + st * SB);
+    const int kc0 = kbeg + i * KC;
     uint4 wv[TN];
 #pragma unroll
     for (int ti = 0; ti < TN; ++ti)
-      wv[ti] = (warp * TN + ti) < ntiles ? lds128(base + (warp * TN + ti) * 512 + lane * 16) : make_uint4(0, 0, 0, 0);
+      wv[ti] = (wt0 + ti) < ntiles ? lds128(base + (wt0 + ti) * 512 + lane * 16) : make_uint4(0, 0, 0, 0);
 
 #pragma unroll
-    for (int ks = 0; ks < G::KS; ++ks) {
+    for (int ks = 0; ks < KS; ++ks) {
+      if constexpr (GROUPED) {
+        const bool maybe = FOLD == 0 ? (ks == 0) : FOLD > 0 ? (ks % (FOLD > 0 ? FOLD : 1) == 0) : true;
+        if (maybe && kc0 + ks * 16 == next_fold) {  // a group ended before this k-step
+          fold(cur_g);
+          ++cur_g;
+          next_fold = min(next_fold + p.gs, kend);
+          set_zeros(cur_g);
+        }
+      }
       uint32_t b[MT][2];
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt) {
-        const uint2 v = lds64(base + L::kXOff + (mt * 8 + g) * XP + ks * 32 + t * 8);
+        const uint2 v = lds64(base + L.x_off() + (mt * 8 + g) * XP + ks * 32 + t * 8);
         b[mt][0] = v.x;
         b[mt][1] = v.y;
-        if (GROUPED) {
-          constexpr uint32_t one = Magic<BF16>::kOnePair;
-          mma16816<BF16>(xs[mt], one, one, one, one, v.x, v.y);
-        }
       }
-      const int h = ks / G::WK, j = ks % G::WK;
+      const int h = ks / WK, j = ks % WK;
 #pragma unroll
       for (int ti = 0; ti < TN; ++ti) {
         const uint32_t wg = h ? wv[ti].z : wv[ti].x;
@@ -289,10 +280,10 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_min_blocks(MT, TN))
           a2 = int8_pair<BF16>(wg, 1);
           a3 = int8_pair<BF16>(wg8, 1);
         } else {
-          a0 = code_pair<W, BF16>(wg, 2 * j);
-          a1 = code_pair<W, BF16>(wg8, 2 * j);
-          a2 = code_pair<W, BF16>(wg, 2 * j + 1);
-          a3 = code_pair<W, BF16>(wg8, 2 * j + 1);
+          a0 = sub_pair<BF16>(code_pair<W, BF16>(wg, 2 * j), zz[ti][0]);
+          a1 = sub_pair<BF16>(code_pair<W, BF16>(wg8, 2 * j), zz[ti][1]);
+          a2 = sub_pair<BF16>(code_pair<W, BF16>(wg, 2 * j + 1), zz[ti][0]);
+          a3 = sub_pair<BF16>(code_pair<W, BF16>(wg8, 2 * j + 1), zz[ti][1]);
         }
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
@@ -302,47 +293,21 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_min_blocks(MT, TN))
             mma16816<BF16>(acc[ti][mt], a0, a1, a2, a3, b[mt][0], b[mt][1]);
         }
       }
-      if (GROUPED && (--kleft == 0 || i * G::KS + ks + 1 == ksteps)) {
-        // Group done: fold P and X of this group into the output accumulators.
-        mbar_wait(smem_addr(&ready[st]), (i / STAGES) & 1, p.err, &s_abort);
-        const int r = gi - gi_stage;  // group row inside this stage
-        const uint32_t prow = base + poff + r * L::kPRow;
-#pragma unroll
-        for (int ti = 0; ti < TN; ++ti)
-#pragma unroll
-          for (int rr = 0; rr < 2; ++rr) {
-            const float2 sz = lds64f(prow + ((warp * TN + ti) * 16 + g + 8 * rr) * 8);
-#pragma unroll
-            for (int mt = 0; mt < MT; ++mt) {
-              float *a = &acc[ti][mt][2 * rr];
-              float *pg = &accg[ti][mt][2 * rr];
-              a[0] = fmaf(sz.y, xs[mt][0], fmaf(sz.x, pg[0], a[0]));
-              a[1] = fmaf(sz.y, xs[mt][1], fmaf(sz.x, pg[1], a[1]));
-              pg[0] = 0.f;
-              pg[1] = 0.f;
-            }
-          }
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) xs[mt][e] = 0.f;
-        ++gi;
-        kleft = p.kspg;
-      }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_addr(&empty[st]));
   }
+  if constexpr (GROUPED) fold(cur_g);
 
   // -------------------------------------------------------------- epilogue
   const float *sc32 = static_cast<const float *>(p.scales);
   float *dst = p.splits == 1 ? p.out : p.partial + (size_t)split * p.M * p.N;
 #pragma unroll
   for (int ti = 0; ti < TN; ++ti) {
-    if (warp * TN + ti >= ntiles) continue;
+    if (wt0 + ti >= ntiles) continue;
 #pragma unroll
     for (int rr = 0; rr < 2; ++rr) {
-      const int n = n0 + (warp * TN + ti) * 16 + g + 8 * rr;
+      const int n = n0 + (wt0 + ti) * 16 + g + 8 * rr;
       const float s8 = (W == 8 && p.splits == 1) ? __ldg(sc32 + n) : 1.f;
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt)
@@ -371,15 +336,15 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_min_blocks(MT, TN))
     for (int sp0 = 0; sp0 < p.splits; sp0 += 8) {
       const int cnt = min(8, p.splits - sp0);
 #pragma unroll
-      for (int u = 0; u < 8; ++u)
-        if (u < cnt) part[u] = __ldcg(reinterpret_cast<const float4 *>(p.partial + ((size_t)(sp0 + u) * p.M + m) * p.N + n));
+      for (int q = 0; q < 8; ++q)
+        if (q < cnt) part[q] = __ldcg(reinterpret_cast<const float4 *>(p.partial + ((size_t)(sp0 + q) * p.M + m) * p.N + n));
 #pragma unroll
-      for (int u = 0; u < 8; ++u)
-        if (u < cnt) {
-          v.x += part[u].x;
-          v.y += part[u].y;
-          v.z += part[u].z;
-          v.w += part[u].w;
+      for (int q = 0; q < 8; ++q)
+        if (q < cnt) {
+          v.x += part[q].x;
+          v.y += part[q].y;
+          v.z += part[q].z;
+          v.w += part[q].w;
         }
     }
     if (W == 8) {
@@ -394,10 +359,10 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_min_blocks(MT, TN))
   if (threadIdx.x == 0) p.counters[nb] = 0;
 }
 
-template <int W, bool BF16, int MT, int TN, bool ZERO>
+template <int W, bool BF16, int MT, int TN, bool ZERO, int FOLD>
 cudaError_t launch_decode_t(const DecodeParams &dp, const DecodePlan &p, cudaStream_t s) {
-  auto kern = decode_kernel<W, BF16, MT, TN, ZERO>;
-  const int smem = kDecodeHeader + decode_stages(TN) * dp.stage_bytes;
+  auto kern = decode_kernel<W, BF16, MT, TN, ZERO, FOLD>;
+  const int smem = p.smem;
   static int attr_bytes[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -411,11 +376,13 @@ cudaError_t launch_decode_t(const DecodeParams &dp, const DecodePlan &p, cudaStr
   return cudaGetLastError();
 }
 
-// Per-W launcher (one translation unit per W keeps the build parallel).
-template <int W>
-cudaError_t launch_decode_w(const DecodeParams &dp, const DecodePlan &p, bool bf16, bool zero, cudaStream_t s);
+// Launcher for one code width and group schedule (decode_inst.cu, compiled
+// once per pair the build lists).
+template <int W, int FOLD>
+cudaError_t launch_decode_wf(const DecodeParams &dp, const DecodePlan &p, bool bf16, bool zero, cudaStream_t s);
 
-#define WQ_DECODE_CASE(W, BF, MT, TN, Z) \
-  if (bf16 == BF && zero == Z && p.mt == MT && p.tn == TN) return launch_decode_t<W, BF, MT, TN, Z>(dp, p, s);
+#define WQ_DECODE_CASE(W, BF, MT, TN, Z, F)                               \
+  if (bf16 == BF && zero == Z && p.mt == MT && p.tn == TN && p.fold == F) \
+    return launch_decode_t<W, BF, MT, TN, Z, F>(dp, p, s);
 
 }  // namespace wq

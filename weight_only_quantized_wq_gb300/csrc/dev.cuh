@@ -13,18 +13,16 @@ namespace wq {
 // Bits recorded in the library's device status word.
 constexpr uint32_t kDevErrTimeout = 1u;
 
-// A barrier wait gives up after this many nanoseconds of wall-clock time.
-constexpr uint64_t kWaitLimitNs = 4000000000ull;
+// A barrier wait gives up after this many SM clock cycles (about 4 s at the
+// 2.07 GHz maximum clock; longer at lower clocks).  The SM cycle counter is
+// read instead of %globaltimer: a %globaltimer read can stall for a large
+// part of a microsecond, which would be paid on every wait that misses.
+constexpr long long kWaitLimitCycles = 8000000000ll;
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-__device__ __forceinline__ uint64_t global_timer_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
 
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
@@ -74,18 +72,18 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Wait for the phase of `bar` with the given parity to complete.  Gives up
-// after kWaitLimitNs, records kDevErrTimeout in *err, raises the CTA's abort
+// after kWaitLimitCycles, records kDevErrTimeout in *err, raises the CTA's abort
 // flag and returns false.  When `abort` is given, a raised flag (another
 // thread of the CTA gave up) also ends the wait at once; waits that must see
 // their copies land before the CTA exits pass nullptr.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t *err, volatile int *abort) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
+  const long long t0 = clock64();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 255u) == 0u) {
       if (abort && *abort) return false;
-      if (global_timer_ns() - t0 > kWaitLimitNs) {
+      if (clock64() - t0 > kWaitLimitCycles) {
         atomicOr(err, kDevErrTimeout);
         if (abort) *abort = 1;
         return false;
@@ -209,6 +207,17 @@ template <int W_BIT, bool BF16>
 __device__ __forceinline__ uint32_t code_pair(uint32_t w, int i) {
   constexpr uint32_t mask = W_BIT == 4 ? 0x000F000Fu : 0x00030003u;
   return and_or(w >> (W_BIT * i), mask, Magic<BF16>::kPair);
+}
+
+// Both 16-bit halves a - b (fp16 or bf16 pairs, round to nearest even).
+template <bool BF16>
+__device__ __forceinline__ uint32_t sub_pair(uint32_t a, uint32_t b) {
+  uint32_t d;
+  if constexpr (BF16)
+    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  else
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
 }
 
 // Signed int8 bytes (lo, hi) of a word -> exact fp16/bf16 pair.

@@ -22,15 +22,18 @@ struct MatmulArgs {
   uint32_t *err;          // device status word
 };
 
-// Split of the decode kernel over the GPU, chosen on the host.
+// Split of a few-token kernel over the GPU, chosen on the host.
 struct DecodePlan {
+  int srows;     // scale rows one CTA stages in shared memory
+  int zrows;     // zero-word rows one CTA stages in shared memory
+  int smem;      // dynamic shared memory bytes
   int mt;        // 8-row token tiles (1, 2, 4, 8)
   int tn;        // 16-row weight tiles per warp
   int nblocks;   // CTAs along N
   int splits;    // CTAs along K
   int cps;       // chunk rows per split
-  int gcap;      // most groups one chunk row touches (scale / zero rows per stage)
-  int stage_bytes;
+  int fold;      // group schedule: k-steps per group when it divides the chunk, 0 when groups
+                 // end on chunk boundaries, -1 otherwise
   size_t workspace;  // bytes: counters, then splits * M * N fp32 partials (0 if splits == 1)
 };
 
