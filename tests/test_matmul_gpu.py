@@ -139,12 +139,26 @@ def test_zero_rows_is_noop_and_canaries():
 
 
 def test_workspace_too_small_is_rejected():
-    p = syn.int4_sym_decode()
+    # one column block over a long K: more K splits than one cluster reduces,
+    # so the partial sums need the caller's workspace
+    p = syn.grouped("int4-asym narrow", 4, 8192, 64, 4, 128, "bf16", "bf16", (0.002, 0.02), seed=5)
     need = wq.wq_workspace_bytes(p.M, p.N, p.K, 4, p.group_size)
-    if need == 0:
-        pytest.skip("this shape needs no workspace on this GPU")
+    assert need > 0
     d = to_device(p)
     small = torch.zeros(need - 16, dtype=torch.uint8, device="cuda")
     with pytest.raises(wq.WQError) as e:
-        wq.wq_matmul(d["x"], d["packed"], d["scales"], None, p.M, p.N, p.K, 4, p.group_size, workspace=small)
+        wq.wq_matmul(d["x"], d["packed"], d["scales"], d["zeros"], p.M, p.N, p.K, 4, p.group_size, workspace=small)
     assert e.value.status == 7
+    # with enough workspace the same call matches the oracle
+    y = run(p, d).cpu().numpy()
+    assert_close(y, oracle_y(p), p.K, p.name)
+
+
+def test_cluster_split_needs_no_workspace():
+    # few column blocks over a long K: the K splits are reduced inside a
+    # thread-block cluster, so no workspace is needed, and the result matches
+    p = syn.grouped("int4-asym cluster split", 8, 8192, 2048, 4, 128, "bf16", "bf16", (0.002, 0.02), seed=6)
+    assert wq.wq_workspace_bytes(p.M, p.N, p.K, 4, p.group_size) == 0
+    d = to_device(p)
+    y = run(p, d).cpu().numpy()
+    assert_close(y, oracle_y(p), p.K, p.name)

@@ -14,8 +14,14 @@ from tests.helpers import assert_close, to_device
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("make", [syn.int4_sym_decode, syn.int2_asym, syn.int8_per_channel],
-                         ids=["int4_sym_decode", "int2_asym", "int8_per_channel"])
+def _narrow():
+    # One column block over a long K: more K splits than one thread-block
+    # cluster reduces, so the partial sums go through the scratch memory.
+    return syn.grouped("int4-asym narrow", 4, 8192, 64, 4, 128, "bf16", "bf16", (0.002, 0.02), seed=5)
+
+
+@pytest.mark.parametrize("make", [_narrow, syn.int4_sym_decode, syn.int2_asym, syn.int8_per_channel],
+                         ids=["narrow_long_k", "int4_sym_decode", "int2_asym", "int8_per_channel"])
 def test_noalloc_matches_workspace_entry_point_twice(make):
     p = make()
     d = to_device(p)
@@ -31,6 +37,6 @@ def test_noalloc_matches_workspace_entry_point_twice(make):
 
 
 def test_noalloc_scratch_is_used_by_a_split_problem():
-    # the decode workload splits K across CTAs, so the scratch path really runs
-    p = syn.int4_sym_decode()
+    # the narrow problem splits K too finely for a cluster, so the scratch path really runs
+    p = _narrow()
     assert wq.wq_workspace_bytes(p.M, p.N, p.K, p.w_bit, p.group_size) > 0

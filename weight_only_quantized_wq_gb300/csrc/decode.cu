@@ -83,10 +83,13 @@ DecodePlan plan_decode(int M, int N, int K, int w_bit, int group_size, bool zero
   const int gs = (w_bit == 8 || group_size <= 0) ? K : group_size;
   const bool grouped = w_bit != 8;
   const int V = 32 / w_bit;
-  int tns[2] = {4, 2};
-  int ntn = 2;
-  if (mt == 4) { tns[0] = 2; ntn = 1; }
-  if (mt == 8) { tns[0] = 1; ntn = 1; }
+  // Tile columns per warp: two (the CTA covers 128 channels) keep three CTAs
+  // of four consumer warps on an SM; int2 codes with one token tile take four
+  // (their long chunk rows make the activation loads per tile the larger cost).
+  // 64-row slices use one.
+  int tns[1] = {w_bit == 2 && mt == 1 ? 4 : 2};
+  const int ntn = 1;
+  if (mt == 8) tns[0] = 1;
   double best_cost = 1e300;
   for (int a = 0; a < ntn; ++a) {
     const int tn = tns[a];
@@ -110,8 +113,10 @@ DecodePlan plan_decode(int M, int N, int K, int w_bit, int group_size, bool zero
       // weight bytes the busiest SM streams (one wave if the units fit the slots)
       const long per_sm = units <= slots ? (units + sms - 1) / sms : ((units + slots - 1) / slots) * occ;
       double cost = (double)per_sm * (cps * (double)tn * kDecodeWarps * 512.0 + 8192.0);
-      // the partial sums' round trip, spread over the SMs
-      if (sreal > 1) cost += 8.0 * rows * (double)N * sreal / sms;
+      // split-K: reduction in the cluster's shared memory (up to 16 splits), or
+      // the partial sums' round trip through the workspace
+      if (sreal > 1 && sreal <= kMaxClusterSplits) cost += 2.0 * rows * (double)N * sreal / sms;
+      if (sreal > kMaxClusterSplits) cost += 8.0 * rows * (double)N * sreal / sms;
       if (cost < best_cost * 0.999) {
         best_cost = cost;
         best.mt = mt;
@@ -126,7 +131,10 @@ DecodePlan plan_decode(int M, int N, int K, int w_bit, int group_size, bool zero
     }
   }
   best.fold = fold_for(w_bit, gs);
-  best.workspace = best.splits > 1 ? decode_counter_bytes() + (size_t)best.splits * rows * N * sizeof(float) : 0;
+  best.cluster = best.splits > 1 && best.splits <= kMaxClusterSplits;
+  best.workspace = best.splits > kMaxClusterSplits
+                       ? decode_counter_bytes() + (size_t)best.splits * rows * N * sizeof(float)
+                       : 0;
   return best;
 }
 
@@ -148,7 +156,8 @@ cudaError_t launch_decode(const MatmulArgs &a, const DecodePlan &p, void *worksp
   dp.srows = p.srows;
   dp.zrows = p.zrows;
   dp.s_bf16 = a.s_bf16;
-  if (p.splits > 1) {
+  dp.cluster = p.cluster;
+  if (p.splits > 1 && !p.cluster) {
     dp.counters = static_cast<int *>(workspace);
     dp.partial = reinterpret_cast<float *>(static_cast<char *>(workspace) + decode_counter_bytes());
   }

@@ -31,10 +31,15 @@
 // for any other multiple of 16.  A CTA's K range may end inside a group
 // (split-K); that partial group is folded at the range's end.
 //
-// Split-K: when the column blocks alone leave SMs idle, the K range is split;
-// each CTA writes its fp32 partial to the workspace and the last CTA to
-// arrive for a column block (atomic counter, no waiting) adds the partials in
-// split order, so the result does not depend on arrival order.
+// Split-K: when the column blocks alone leave SMs idle, the K range is split.
+// Up to 16 splits of a column block form one thread-block cluster: every CTA
+// leaves its fp32 partial tile in its own shared memory, and after a cluster
+// barrier each CTA sums one slice of the tile over the cluster's CTAs
+// (distributed shared memory, split order) and writes it -- no global
+// round trip, no workspace.  Beyond 16 splits each CTA writes its partial to
+// the workspace and the last CTA to arrive for a column block (atomic
+// counter, no waiting) adds the partials in split order.  Either way the
+// result does not depend on arrival order.
 #pragma once
 
 #include <cstdint>
@@ -87,6 +92,7 @@ struct DecodeParams {
   uint32_t *err;
   int M, N, K, gs, nt_total, kch, splits, cps, srows, zrows;
   bool s_bf16;
+  bool cluster;  // the splits of a column block form a cluster (reduction in shared memory)
 };
 
 __device__ __forceinline__ void consumer_sync() {
@@ -161,6 +167,11 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_min_blocks(MT, TN))
       // No copy may still be writing this CTA's shared memory when it exits.
       for (int i = max(0, issued - STAGES); i < issued; ++i)
         mbar_wait(smem_addr(&full[i % STAGES]), (i / STAGES) & 1, p.err, nullptr);
+    }
+    __syncwarp();
+    if (p.cluster) {  // the consumers' two cluster barriers
+      cluster_sync();
+      cluster_sync();
     }
     return;
   }
@@ -301,6 +312,50 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_min_blocks(MT, TN))
 
   // -------------------------------------------------------------- epilogue
   const float *sc32 = static_cast<const float *>(p.scales);
+  if (p.cluster) {
+    // Partial tile -> own shared memory (the ring is free: every stage was consumed).
+    constexpr int RP = CC + 4;  // row pitch (floats): fragment stores are conflict-free
+    const uint32_t red = smem_addr(ring);
+    consumer_sync();
+#pragma unroll
+    for (int ti = 0; ti < TN; ++ti)
+#pragma unroll
+      for (int rr = 0; rr < 2; ++rr)
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            const int m = mt * 8 + 2 * t + c;
+            if (m < p.M) sts_f32(red + (m * RP + (wt0 + ti) * 16 + g + 8 * rr) * 4, acc[ti][mt][2 * rr + c]);
+          }
+    cluster_sync();
+    // This CTA's slice of the tile, summed over the cluster in split order.
+    const uint32_t rank = cluster_ctarank();
+    const int qpr = ntiles * 4;  // float4 quads per row
+    const int nq = p.M * qpr;
+    for (int q = threadIdx.x * p.splits + (int)rank; q < nq; q += NW * 32 * p.splits) {
+      const int m = q / qpr, col = (q % qpr) * 4;
+      const uint32_t la = red + (m * RP + col) * 4;
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int r = 0; r < p.splits; ++r) {
+        const float4 u = ld_dsmem_f4(dsmem_addr(la, (uint32_t)r));
+        v.x += u.x;
+        v.y += u.y;
+        v.z += u.z;
+        v.w += u.w;
+      }
+      if (W == 8) {
+        const float4 s4 = __ldg(reinterpret_cast<const float4 *>(sc32 + n0 + col));
+        v.x *= s4.x;
+        v.y *= s4.y;
+        v.z *= s4.z;
+        v.w *= s4.w;
+      }
+      *reinterpret_cast<float4 *>(p.out + (size_t)m * p.N + n0 + col) = v;
+    }
+    cluster_sync();  // no CTA leaves while another still reads its shared memory
+    return;
+  }
   float *dst = p.splits == 1 ? p.out : p.partial + (size_t)split * p.M * p.N;
 #pragma unroll
   for (int ti = 0; ti < TN; ++ti) {
@@ -371,9 +426,26 @@ cudaError_t launch_decode_t(const DecodeParams &dp, const DecodePlan &p, cudaStr
     if (e != cudaSuccess) return e;
     attr_bytes[dev] = smem;
   }
-  dim3 grid(p.nblocks, p.splits);
-  kern<<<grid, kDecodeThreads, smem, s>>>(dp);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(p.nblocks, p.splits);
+  cfg.blockDim = dim3(kDecodeThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  if (dp.cluster) {
+    if (p.splits > 8) {
+      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      if (e != cudaSuccess) return e;
+    }
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = p.splits;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, dp);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 // Launcher for one code width and group schedule (decode_inst.cu, compiled

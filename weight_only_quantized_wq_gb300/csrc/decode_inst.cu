@@ -15,7 +15,6 @@ cudaError_t launch_decode_wf<WQ_W, WQ_FOLD>(const DecodeParams &dp, const Decode
 #define SHAPES(BF, Z)                       \
   WQ_DECODE_CASE(WQ_W, BF, 1, 4, Z, WQ_FOLD) \
   WQ_DECODE_CASE(WQ_W, BF, 1, 2, Z, WQ_FOLD) \
-  WQ_DECODE_CASE(WQ_W, BF, 2, 4, Z, WQ_FOLD) \
   WQ_DECODE_CASE(WQ_W, BF, 2, 2, Z, WQ_FOLD) \
   WQ_DECODE_CASE(WQ_W, BF, 4, 2, Z, WQ_FOLD) \
   WQ_DECODE_CASE(WQ_W, BF, 8, 1, Z, WQ_FOLD)

@@ -32,10 +32,14 @@ struct DecodePlan {
   int nblocks;   // CTAs along N
   int splits;    // CTAs along K
   int cps;       // chunk rows per split
+  bool cluster;  // the splits of a column block form a cluster (reduction in shared memory)
   int fold;      // group schedule: k-steps per group when it divides the chunk, 0 when groups
                  // end on chunk boundaries, -1 otherwise
   size_t workspace;  // bytes: counters, then splits * M * N fp32 partials (0 if splits == 1)
 };
+
+// Most K splits whose partial tiles are reduced inside one thread-block cluster.
+constexpr int kMaxClusterSplits = 16;
 
 // Arrival counters at the start of every workspace (one per column block).
 constexpr int kMaxColumnBlocks = 4096;
