@@ -288,18 +288,23 @@ def sample_cols(p, target_cols_frac=1.0):
     return max(16, int(p.N * target_cols_frac) // 16 * 16)
 
 
-def cpu_measure(p, steps, warmup):
-    """Time the oracle on a column sample; returns (GB/s of weight bytes covered, cores, sample text)."""
+def cpu_measure(p, steps, warmup, min_seconds=0.0):
+    """Time the oracle on a column sample; returns (GB/s of weight bytes covered,
+    cores, sample text, seconds per step).  At least `steps` steps, and more
+    (up to 200) until `min_seconds` of CPU work have been timed."""
     threads = os.cpu_count() or 1
     ncols = sample_cols(p)
     for _ in range(warmup):
         oracle_step(p, ncols, threads)
     t0 = time.perf_counter()
-    for _ in range(steps):
+    done = 0
+    while done < steps or (time.perf_counter() - t0 < min_seconds and done < 200):
         oracle_step(p, ncols, threads)
-    dt = (time.perf_counter() - t0) / steps
+        done += 1
+    dt = (time.perf_counter() - t0) / done
     wbytes = p.weight_bytes() * ncols / p.N
-    sample = "all %d rows x first %d of %d columns (K=%d) per step" % (p.M, ncols, p.N, p.K)
+    sample = "all %d rows x first %d of %d columns (K=%d) per step, %d steps (%.1f s)" % (
+        p.M, ncols, p.N, p.K, done, dt * done)
     return wbytes / dt / 1e9, threads, sample, dt
 
 
@@ -404,7 +409,7 @@ def main():
         if not args.no_sweep and not args.kernel_only:
             line["sweep"] = sweep(torch, wq, syn, l2, pk, pk_src)
         if not args.kernel_only:
-            gbps, cores, sample, _ = cpu_measure(p, 1, 0)
+            gbps, cores, sample, _ = cpu_measure(p, 1, 1, min_seconds=10.0)
             line["cpu_baseline"] = {"value": round(gbps, 3), "unit": UNIT, "cores": cores, "kind": "oracle",
                                     "sample": sample}
         print(json.dumps(line))
