@@ -34,25 +34,30 @@ namespace wq {
 namespace pf {
 
 constexpr int UM = 128;   // UMMA M (tokens per accumulator)
-constexpr int MSUB = 2;   // accumulators per CTA
-constexpr int BM = UM * MSUB;  // tokens per CTA
 constexpr int BN = 256;   // output channels per CTA (UMMA N)
 constexpr int BK = 64;    // K per stage: one 128-byte swizzle atom of bf16
 constexpr int STAGES = 3;
 constexpr int BSTAGES = 2;            // dequantized B buffers
 constexpr int DQ_WARPS = 8;
 constexpr int THREADS = (2 + DQ_WARPS) * 32;
-constexpr int A_BYTES = BM * BK * 2;  // 32 KB
 constexpr int B_BYTES = BN * BK * 2;  // 32 KB
 constexpr int W_BYTES = BN * BK / 2;  // 8 KB of packed int4
 constexpr int S_BYTES = BN * 2;       // one scale row
 constexpr int Z_BYTES = BN * 4;       // one zero-word row
-// stage = A | W | S | Z, 1024-byte aligned (the swizzle atom of A)
-constexpr int ST_A = 0, ST_W = A_BYTES, ST_S = ST_W + W_BYTES, ST_Z = ST_S + S_BYTES;
-constexpr int STAGE_BYTES = (ST_Z + Z_BYTES + 1023) / 1024 * 1024;
 constexpr int HEADER = 1024;          // mbarriers + TMEM address
-constexpr int SMEM = HEADER + STAGES * STAGE_BYTES + BSTAGES * B_BYTES;
-constexpr int TMEM_COLS = BN * MSUB;  // 512
+
+// Geometry for MS accumulators of 128 tokens each (token tile BM = 128 MS).
+template <int MS>
+struct Cfg {
+  static constexpr int MSUB = MS;
+  static constexpr int BM = UM * MS;                  // tokens per CTA
+  static constexpr int A_BYTES = BM * BK * 2;         // x tile: 16 or 32 KB
+  // stage = A | W | S | Z, 1024-byte aligned (the swizzle atom of A)
+  static constexpr int ST_A = 0, ST_W = A_BYTES, ST_S = ST_W + W_BYTES, ST_Z = ST_S + S_BYTES;
+  static constexpr int STAGE_BYTES = (ST_Z + Z_BYTES + 1023) / 1024 * 1024;
+  static constexpr int SMEM = HEADER + STAGES * STAGE_BYTES + BSTAGES * B_BYTES;
+  static constexpr int TMEM_COLS = BN * MS;           // 256 or 512
+};
 
 struct Params {
   CUtensorMap tm_x;  // x (M, K) 16-bit, box (64, 256), 128-byte swizzle
@@ -144,8 +149,11 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-template <bool BF16, bool ZERO>
+template <bool BF16, bool ZERO, int MS>
 __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_constant__ Params p) {
+  using C = Cfg<MS>;
+  constexpr int MSUB = C::MSUB, BM = C::BM, A_BYTES = C::A_BYTES, STAGE_BYTES = C::STAGE_BYTES;
+  constexpr int ST_A = C::ST_A, ST_W = C::ST_W, ST_S = C::ST_S, ST_Z = C::ST_Z, TMEM_COLS = C::TMEM_COLS;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte alignment (of the shared-window address) for the swizzled tiles
   uint8_t *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
@@ -352,13 +360,13 @@ bool prefill_supported(const MatmulArgs &a) {
   return a.w_bit == 4 && a.group_size % pf::BK == 0 && a.K % pf::BK == 0 && a.x_bf16 == a.s_bf16;
 }
 
-template <bool BF16, bool ZERO>
+template <bool BF16, bool ZERO, int MS>
 static cudaError_t launch_t(const pf::Params &pp, dim3 grid, cudaStream_t s) {
-  auto kern = pf::prefill_kernel<BF16, ZERO>;
+  auto kern = pf::prefill_kernel<BF16, ZERO, MS>;
   static int attr_set[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
-  const int smem = pf::SMEM + 1024;  // + slack for the 1024-byte alignment of the ring
+  const int smem = pf::Cfg<MS>::SMEM + 1024;  // + slack for the 1024-byte alignment of the ring
   if (dev >= 0 && dev < 64 && !attr_set[dev]) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
@@ -368,10 +376,19 @@ static cudaError_t launch_t(const pf::Params &pp, dim3 grid, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+template <int MS>
+static cudaError_t launch_ms(const pf::Params &pp, dim3 grid, bool bf16, bool z, cudaStream_t s) {
+  if (bf16) return z ? launch_t<true, true, MS>(pp, grid, s) : launch_t<true, false, MS>(pp, grid, s);
+  return z ? launch_t<false, true, MS>(pp, grid, s) : launch_t<false, false, MS>(pp, grid, s);
+}
+
 cudaError_t launch_prefill(const MatmulArgs &a, cudaStream_t s) {
   pf::Params pp{};
   const int G = a.K / a.group_size;
-  if (!enc(&pp.tm_x, a.x, 2, (uint64_t)a.K, (uint64_t)a.M, pf::BK, pf::BM, CU_TENSOR_MAP_SWIZZLE_128B))
+  // One 128-token accumulator per CTA up to 128 tokens, two (256 tokens) beyond.
+  const int ms = a.M <= pf::UM ? 1 : 2;
+  const int bm = pf::UM * ms;
+  if (!enc(&pp.tm_x, a.x, 2, (uint64_t)a.K, (uint64_t)a.M, pf::BK, (uint32_t)bm, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   if (!enc(&pp.tm_s, a.scales, 2, (uint64_t)a.N, (uint64_t)G, pf::BN, 1, CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;
@@ -386,10 +403,9 @@ cudaError_t launch_prefill(const MatmulArgs &a, cudaStream_t s) {
   pp.K = a.K;
   pp.gs = a.group_size;
   pp.nt_total = a.N / 16;
-  dim3 grid((a.M + pf::BM - 1) / pf::BM, (a.N + pf::BN - 1) / pf::BN);
+  dim3 grid((a.M + bm - 1) / bm, (a.N + pf::BN - 1) / pf::BN);
   const bool z = a.zeros != nullptr;
-  if (a.x_bf16) return z ? launch_t<true, true>(pp, grid, s) : launch_t<true, false>(pp, grid, s);
-  return z ? launch_t<false, true>(pp, grid, s) : launch_t<false, false>(pp, grid, s);
+  return ms == 1 ? launch_ms<1>(pp, grid, a.x_bf16, z, s) : launch_ms<2>(pp, grid, a.x_bf16, z, s);
 }
 
 }  // namespace wq
