@@ -101,7 +101,7 @@ DecodePlan plan_decode(int M, int N, int K, int w_bit, int group_size, bool zero
       if (s != sreal) continue;
       int srows = 0, zrows = 0;
       if (grouped) rows_for(K, kc, gs, cps, V, &srows, &zrows);
-      if (!zero) zrows = 0;
+      zrows = zero ? srows : 0;  // one (MAGIC + zero) row per group
       const int smem = DecodeSmem{w_bit, mt, tn, srows, zrows}.bytes();
       if (smem > 200 * 1024) continue;
       int occ = decode_min_blocks(mt, tn);  // the register budget the kernel is compiled for

@@ -55,8 +55,8 @@ namespace wq {
 constexpr int kDecodeWarps = 4;  // consumer warps per CTA (plus one producer warp)
 constexpr int kDecodeThreads = (kDecodeWarps + 1) * 32;
 constexpr int kDecodeHeader = 256;  // mbarriers in front of the staged rows
-// Ring depth: about 40 KB of weights in flight per CTA.
-__host__ __device__ constexpr int decode_stages(int tn) { return tn >= 4 ? 5 : 8; }
+// Ring depth: 24 to 40 KB of weights in flight per CTA.
+__host__ __device__ constexpr int decode_stages(int tn) { return tn >= 4 ? 5 : 6; }
 // Resident CTAs per SM the register budget is sized for.
 __host__ __device__ constexpr int decode_min_blocks(int mt, int tn) { return mt * tn >= 8 ? 2 : 3; }
 
@@ -66,13 +66,15 @@ __host__ __device__ constexpr int align128(int v) { return (v + 127) / 128 * 128
 // is 8 mod 32, which makes the 8-byte B-fragment loads of a warp conflict-free.
 __host__ __device__ constexpr int x_pitch(int w) { return 4 * ((128 / w) + ((8 - (128 / w) % 32) + 32) % 32); }
 
-// Shared-memory layout of one CTA: barriers | staged scale rows | staged
-// zero-word rows | ring of stages (packed weights, then the activation slice).
+// Shared-memory layout of one CTA: barriers | staged scales (fp32, one row per
+// group) | staged (MAGIC + zero) pairs (one row per group, asymmetric codes
+// only: zrows = srows, else 0) | ring of stages (packed weights, then the
+// activation slice).
 struct DecodeSmem {
   int w, mt, tn, srows, zrows;
   __host__ __device__ constexpr int cols() const { return kDecodeWarps * tn * 16; }
   __host__ __device__ constexpr int s_off() const { return kDecodeHeader; }
-  __host__ __device__ constexpr int z_off() const { return align128(s_off() + srows * cols() * 2); }
+  __host__ __device__ constexpr int z_off() const { return align128(s_off() + srows * cols() * 4); }
   __host__ __device__ constexpr int ring_off() const { return align128(z_off() + zrows * cols() * 4); }
   __host__ __device__ constexpr int w_bytes() const { return cols() * 32; }  // one chunk row of weights
   __host__ __device__ constexpr int x_off() const { return w_bytes(); }
@@ -122,8 +124,8 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_min_blocks(MT, TN))
   uint64_t *full = reinterpret_cast<uint64_t *>(smem);
   uint64_t *empty = full + STAGES;
   static_assert(2 * STAGES * 8 <= kDecodeHeader, "barriers do not fit the header");
-  const uint16_t *s_sm = reinterpret_cast<const uint16_t *>(smem + L.s_off());  // [srows][CC]
-  const uint32_t *z_sm = reinterpret_cast<const uint32_t *>(smem + L.z_off());  // [zrows][CC]
+  const float *s_sm = reinterpret_cast<const float *>(smem + L.s_off());         // [srows][CC] scales
+  const uint32_t *z_sm = reinterpret_cast<const uint32_t *>(smem + L.z_off());  // [zrows][CC] MAGIC + zero pairs
   uint8_t *ring = smem + L.ring_off();
   const int SB = L.stage_bytes();
 
@@ -139,7 +141,7 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_min_blocks(MT, TN))
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
       mbar_init(smem_addr(&full[i]), 1);
-      mbar_init(smem_addr(&empty[i]), NW);
+      mbar_init(smem_addr(&empty[i]), NW * 32);  // every consumer lane arrives
     }
     s_abort = 0;
     fence_barrier_init();
@@ -180,24 +182,39 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_min_blocks(MT, TN))
   const int g = lane >> 2, t = lane & 3;
   const int wt0 = warp * TN;  // first tile of this warp within the CTA
 
-  // Scale and zero rows of the CTA's groups -> shared memory (16-byte loads),
-  // while the producer fills the ring.
+  // Scales (as fp32) and (MAGIC + zero) pairs of the CTA's groups -> shared
+  // memory, while the producer fills the ring.
   const int g0 = GROUPED ? kbeg / p.gs : 0;
   if constexpr (GROUPED) {
     const int ng = (kend - 1) / p.gs - g0 + 1;
     const int cols = ntiles * 16;
-    uint16_t *sw = reinterpret_cast<uint16_t *>(smem + L.s_off());
+    float *sw = reinterpret_cast<float *>(smem + L.s_off());
     const uint16_t *sg = static_cast<const uint16_t *>(p.scales);
     for (int idx = threadIdx.x; idx < ng * (cols / 8); idx += NW * 32) {
       const int row = idx / (cols / 8), c = (idx % (cols / 8)) * 8;
-      *reinterpret_cast<uint4 *>(sw + row * CC + c) = ldg_nc128(sg + (size_t)(g0 + row) * p.N + n0 + c);
+      const uint4 h = ldg_nc128(sg + (size_t)(g0 + row) * p.N + n0 + c);
+      const uint32_t hw[4] = {h.x, h.y, h.z, h.w};
+      float f[8];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        f[2 * e] = half_bits_to_float((uint16_t)(hw[e] & 0xFFFFu), p.s_bf16);
+        f[2 * e + 1] = half_bits_to_float((uint16_t)(hw[e] >> 16), p.s_bf16);
+      }
+      *reinterpret_cast<float4 *>(sw + row * CC + c) = make_float4(f[0], f[1], f[2], f[3]);
+      *reinterpret_cast<float4 *>(sw + row * CC + c + 4) = make_float4(f[4], f[5], f[6], f[7]);
     }
     if constexpr (ZERO) {
       uint32_t *zw = reinterpret_cast<uint32_t *>(smem + L.z_off());
-      const int nz = (kend - 1) / p.gs / V - g0 / V + 1;
-      for (int idx = threadIdx.x; idx < nz * (cols / 4); idx += NW * 32) {
+      for (int idx = threadIdx.x; idx < ng * (cols / 4); idx += NW * 32) {
         const int row = idx / (cols / 4), c = (idx % (cols / 4)) * 4;
-        *reinterpret_cast<uint4 *>(zw + row * CC + c) = ldg_nc128(p.zeros + (size_t)(g0 / V + row) * p.N + n0 + c);
+        const int gi = g0 + row;
+        const uint4 w4 = ldg_nc128(p.zeros + (size_t)(gi / V) * p.N + n0 + c);
+        const uint32_t ww[4] = {w4.x, w4.y, w4.z, w4.w};
+        uint32_t zp[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          zp[e] = ((Magic<BF16>::kPair & 0xFFFFu) + ((ww[e] >> ((gi % V) * W)) & ((1u << W) - 1u))) * 0x00010001u;
+        *reinterpret_cast<uint4 *>(zw + row * CC + c) = make_uint4(zp[0], zp[1], zp[2], zp[3]);
       }
     }
     consumer_sync();
@@ -219,10 +236,10 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_min_blocks(MT, TN))
     for (int ti = 0; ti < TN; ++ti)
 #pragma unroll
       for (int rr = 0; rr < 2; ++rr) {
-        uint32_t z = 1u << (W - 1);
         if constexpr (ZERO)
-          z = (z_sm[(gi / V - g0 / V) * CC + (wt0 + ti) * 16 + g + 8 * rr] >> ((gi % V) * W)) & ((1u << W) - 1u);
-        zz[ti][rr] = ((Magic<BF16>::kPair & 0xFFFFu) + z) * 0x00010001u;
+          zz[ti][rr] = z_sm[(gi - g0) * CC + (wt0 + ti) * 16 + g + 8 * rr];
+        else
+          zz[ti][rr] = ((Magic<BF16>::kPair & 0xFFFFu) + (1u << (W - 1))) * 0x00010001u;
       }
   };
   // acc += scale[gi] * (sum over group gi); the group sum restarts.
@@ -231,7 +248,7 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_min_blocks(MT, TN))
     for (int ti = 0; ti < TN; ++ti)
 #pragma unroll
       for (int rr = 0; rr < 2; ++rr) {
-        const float s = half_bits_to_float(s_sm[(gi - g0) * CC + (wt0 + ti) * 16 + g + 8 * rr], p.s_bf16);
+        const float s = s_sm[(gi - g0) * CC + (wt0 + ti) * 16 + g + 8 * rr];
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
@@ -305,8 +322,7 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_min_blocks(MT, TN))
         }
       }
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(smem_addr(&empty[st]));
+    mbar_arrive(smem_addr(&empty[st]));  // this lane is done with the stage
   }
   if constexpr (GROUPED) fold(cur_g);
 
