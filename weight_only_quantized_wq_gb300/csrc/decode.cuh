@@ -155,9 +155,10 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_min_blocks(MT, TN))
     const uint32_t xbytes = (uint32_t)L.x_bytes();
     int issued = 0;
     if (lane == 0) {
+      int st = 0;
+      uint32_t ph = 0;  // phase parity of the ring's current lap
       for (int i = 0; i < nch; ++i) {
-        const int st = i % STAGES;
-        if (i >= STAGES && !mbar_wait(smem_addr(&empty[st]), ((i / STAGES) - 1) & 1, p.err, &s_abort)) break;
+        if (i >= STAGES && !mbar_wait(smem_addr(&empty[st]), ph ^ 1u, p.err, &s_abort)) break;
         const uint32_t fb = smem_addr(&full[st]);
         const uint32_t base = smem_addr(ring + st * SB);
         const int kc = c0 + i;
@@ -165,6 +166,10 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_min_blocks(MT, TN))
         bulk_g2s(base, p.packed + ((size_t)kc * p.nt_total + nt0) * 512, wbytes, fb, pol_w);
         tma_load_2d(base + L.x_off(), &p.tm_x, kc * KC, 0, fb);
         issued = i + 1;
+        if (++st == STAGES) {
+          st = 0;
+          ph ^= 1u;
+        }
       }
       // No copy may still be writing this CTA's shared memory when it exits.
       for (int i = max(0, issued - STAGES); i < issued; ++i)
@@ -267,10 +272,11 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_min_blocks(MT, TN))
   // complete, so a non-blocking test of each stage's barrier is issued one
   // stage early and its answer is only read when that stage starts.
   bool next_ready = nch > 0 && mbar_test_wait(smem_addr(&full[0]), 0);
+  int st = 0, st1 = 1 % STAGES;  // this stage and the next (ring slots)
+  uint32_t ph = 0, ph1 = STAGES == 1 ? 1u : 0u;  // their phase parities
   for (int i = 0; i < nch; ++i) {
-    const int st = i % STAGES;
-    if (!next_ready && !mbar_wait(smem_addr(&full[st]), (i / STAGES) & 1, p.err, &s_abort)) break;
-    if (i + 1 < nch) next_ready = mbar_test_wait(smem_addr(&full[(i + 1) % STAGES]), ((i + 1) / STAGES) & 1);
+    if (!next_ready && !mbar_wait(smem_addr(&full[st]), ph, p.err, &s_abort)) break;
+    if (i + 1 < nch) next_ready = mbar_test_wait(smem_addr(&full[st1]), ph1);
     const uint32_t base = smem_addr(ring + st * SB);
     const int kc0 = kbeg + i * KC;
     uint4 wv[TN];
@@ -323,6 +329,12 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_min_blocks(MT, TN))
       }
     }
     mbar_arrive(smem_addr(&empty[st]));  // this lane is done with the stage
+    st = st1;
+    ph = ph1;
+    if (++st1 == STAGES) {
+      st1 = 0;
+      ph1 ^= 1u;
+    }
   }
   if constexpr (GROUPED) fold(cur_g);
 
