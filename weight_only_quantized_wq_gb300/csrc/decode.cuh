@@ -236,6 +236,9 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_min_blocks(MT, TN))
 
   // (MAGIC + zero) of the current group for rows g and g + 8 of every tile
   uint32_t zz[TN][2];
+  // fp16 int4 only: 960 - (1024 + zero), the fma addend of the odd fields
+  constexpr bool kOddFma = W == 4 && !BF16;
+  uint32_t zz16[TN][2];
   auto set_zeros = [&](int gi) {
 #pragma unroll
     for (int ti = 0; ti < TN; ++ti)
@@ -245,6 +248,7 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_min_blocks(MT, TN))
           zz[ti][rr] = z_sm[(gi - g0) * CC + (wt0 + ti) * 16 + g + 8 * rr];
         else
           zz[ti][rr] = ((Magic<BF16>::kPair & 0xFFFFu) + (1u << (W - 1))) * 0x00010001u;
+        if constexpr (kOddFma) zz16[ti][rr] = sub_pair<false>(kF16NineSixty, zz[ti][rr]);
       }
   };
   // acc += scale[gi] * (sum over group gi); the group sum restarts.
@@ -313,6 +317,13 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_min_blocks(MT, TN))
           a1 = int8_pair<BF16>(wg8, 0);
           a2 = int8_pair<BF16>(wg, 1);
           a3 = int8_pair<BF16>(wg8, 1);
+        } else if constexpr (kOddFma) {
+          // fields 2j and 2j + 1 from one shift by 8 j
+          const uint32_t v = wg >> (8 * j), v8 = wg8 >> (8 * j);
+          a0 = sub_pair<false>(and_or(v, 0x000F000Fu, Magic<false>::kPair), zz[ti][0]);
+          a1 = sub_pair<false>(and_or(v8, 0x000F000Fu, Magic<false>::kPair), zz[ti][1]);
+          a2 = fma_h2(and_or(v, 0x00F000F0u, Magic<false>::kPair), kF16Sixteenth, zz16[ti][0]);
+          a3 = fma_h2(and_or(v8, 0x00F000F0u, Magic<false>::kPair), kF16Sixteenth, zz16[ti][1]);
         } else {
           a0 = sub_pair<BF16>(code_pair<W, BF16>(wg, 2 * j), zz[ti][0]);
           a1 = sub_pair<BF16>(code_pair<W, BF16>(wg8, 2 * j), zz[ti][1]);

@@ -246,21 +246,36 @@ __device__ __forceinline__ uint32_t sub_pair(uint32_t a, uint32_t b) {
   return d;
 }
 
+// Both fp16 halves a * b + c, one rounding.
+__device__ __forceinline__ uint32_t fma_h2(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+// fp16 int4 without the shift for odd fields: masking field 2i + 1 in place
+// gives the fp16 value 1024 + 16 q (16 q stays inside the 10 fraction bits).
+// (1024 + 16 q) * (1/16) - (64 + z) = q - z exactly, in one fma with
+// c = 960 - (1024 + z), built once per group from the (1024 + z) pair.
+constexpr uint32_t kF16Sixteenth = 0x2C002C00u;  // (1/16, 1/16)
+constexpr uint32_t kF16NineSixty = 0x63806380u;  // (960, 960)
+
 // Signed int8 bytes (lo, hi) of a word -> exact fp16/bf16 pair.
 template <bool BF16>
 __device__ __forceinline__ uint32_t int8_pair(uint32_t w, int hi_half) {
-  const uint32_t u = w ^ 0x80808080u;  // unsigned u = q + 128 per byte
   if constexpr (BF16) {
-    // 0x4B0000uu is the fp32 value 2^23 + u; subtract 2^23 + 128.
-    const uint32_t s0 = hi_half ? 0x7442u : 0x7440u;
-    const uint32_t s1 = hi_half ? 0x7443u : 0x7441u;
-    const float f0 = __uint_as_float(__byte_perm(u, 0x4B000000u, s0)) - 8388736.0f;
-    const float f1 = __uint_as_float(__byte_perm(u, 0x4B000000u, s1)) - 8388736.0f;
+    // q = q7 - 128 s (q7 = low seven bits, s = sign bit).  With the bytes in
+    // the low byte of each 16-bit half: (0x4300 | q7) is the bf16 value 128 + q7
+    // and (0x4300 | s << 7) is 128 or 256; their difference is q, exactly.
+    const uint32_t t = __byte_perm(w, 0u, hi_half ? 0x4342u : 0x4140u);
+    const uint32_t a = and_or(t, 0x007F007Fu, Magic<true>::kPair);
+    const uint32_t b = and_or(t, 0x00800080u, Magic<true>::kPair);
     uint32_t r;
-    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(f1), "f"(f0));  // high <- f1, low <- f0
+    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
     return r;
   } else {
-    // 0x64uu is the fp16 value 1024 + u; subtract 1152 from both halves.
+    // 0x64uu is the fp16 value 1024 + u (u = q + 128); subtract 1152 from both halves.
+    const uint32_t u = w ^ 0x80808080u;
     const uint32_t h = __byte_perm(u, 0x64646464u, hi_half ? 0x7362u : 0x5140u);
     uint32_t r;
     asm("sub.f16x2 %0, %1, %2;" : "=r"(r) : "r"(h), "r"(0x64806480u));
