@@ -191,35 +191,73 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_min_blocks(MT, TN))
   // memory, while the producer fills the ring.
   const int g0 = GROUPED ? kbeg / p.gs : 0;
   if constexpr (GROUPED) {
+    constexpr int CT = NW * 32;  // consumer threads
+    constexpr int SB4 = 4;       // loads in flight per thread
     const int ng = (kend - 1) / p.gs - g0 + 1;
     const int cols = ntiles * 16;
     float *sw = reinterpret_cast<float *>(smem + L.s_off());
     const uint16_t *sg = static_cast<const uint16_t *>(p.scales);
-    for (int idx = threadIdx.x; idx < ng * (cols / 8); idx += NW * 32) {
-      const int row = idx / (cols / 8), c = (idx % (cols / 8)) * 8;
-      const uint4 h = ldg_nc128(sg + (size_t)(g0 + row) * p.N + n0 + c);
-      const uint32_t hw[4] = {h.x, h.y, h.z, h.w};
-      float f[8];
+    const int sitems = ng * (cols / 8);  // 8 scales per 16-byte load
+    for (int b0 = 0; b0 < sitems; b0 += SB4 * CT) {
+      uint4 h[SB4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        f[2 * e] = half_bits_to_float((uint16_t)(hw[e] & 0xFFFFu), p.s_bf16);
-        f[2 * e + 1] = half_bits_to_float((uint16_t)(hw[e] >> 16), p.s_bf16);
+      for (int j = 0; j < SB4; ++j) {
+        const int idx = b0 + j * CT + threadIdx.x;
+        if (idx < sitems) {
+          const int row = idx / (cols / 8), c = (idx % (cols / 8)) * 8;
+          h[j] = ldg_nc128(sg + (size_t)(g0 + row) * p.N + n0 + c);
+        }
       }
-      *reinterpret_cast<float4 *>(sw + row * CC + c) = make_float4(f[0], f[1], f[2], f[3]);
-      *reinterpret_cast<float4 *>(sw + row * CC + c + 4) = make_float4(f[4], f[5], f[6], f[7]);
+#pragma unroll
+      for (int j = 0; j < SB4; ++j) {
+        const int idx = b0 + j * CT + threadIdx.x;
+        if (idx < sitems) {
+          const int row = idx / (cols / 8), c = (idx % (cols / 8)) * 8;
+          const uint32_t hw[4] = {h[j].x, h[j].y, h[j].z, h[j].w};
+          float f[8];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            f[2 * e] = half_bits_to_float((uint16_t)(hw[e] & 0xFFFFu), p.s_bf16);
+            f[2 * e + 1] = half_bits_to_float((uint16_t)(hw[e] >> 16), p.s_bf16);
+          }
+          *reinterpret_cast<float4 *>(sw + row * CC + c) = make_float4(f[0], f[1], f[2], f[3]);
+          *reinterpret_cast<float4 *>(sw + row * CC + c + 4) = make_float4(f[4], f[5], f[6], f[7]);
+        }
+      }
     }
     if constexpr (ZERO) {
+      // Each packed zero word holds V groups: read every word row once and
+      // write the (MAGIC + zero) pairs of the groups of this CTA it holds.
       uint32_t *zw = reinterpret_cast<uint32_t *>(smem + L.z_off());
-      for (int idx = threadIdx.x; idx < ng * (cols / 4); idx += NW * 32) {
-        const int row = idx / (cols / 4), c = (idx % (cols / 4)) * 4;
-        const int gi = g0 + row;
-        const uint4 w4 = ldg_nc128(p.zeros + (size_t)(gi / V) * p.N + n0 + c);
-        const uint32_t ww[4] = {w4.x, w4.y, w4.z, w4.w};
-        uint32_t zp[4];
+      const int wr0 = g0 / V, nwr = (g0 + ng - 1) / V - wr0 + 1;
+      const int zitems = nwr * (cols / 4);  // 4 words per 16-byte load
+      for (int b0 = 0; b0 < zitems; b0 += SB4 * CT) {
+        uint4 w4[SB4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-          zp[e] = ((Magic<BF16>::kPair & 0xFFFFu) + ((ww[e] >> ((gi % V) * W)) & ((1u << W) - 1u))) * 0x00010001u;
-        *reinterpret_cast<uint4 *>(zw + row * CC + c) = make_uint4(zp[0], zp[1], zp[2], zp[3]);
+        for (int j = 0; j < SB4; ++j) {
+          const int idx = b0 + j * CT + threadIdx.x;
+          if (idx < zitems) {
+            const int row = idx / (cols / 4), c = (idx % (cols / 4)) * 4;
+            w4[j] = ldg_nc128(p.zeros + (size_t)(wr0 + row) * p.N + n0 + c);
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < SB4; ++j) {
+          const int idx = b0 + j * CT + threadIdx.x;
+          if (idx < zitems) {
+            const int row = idx / (cols / 4), c = (idx % (cols / 4)) * 4;
+            const uint32_t ww[4] = {w4[j].x, w4[j].y, w4[j].z, w4[j].w};
+            for (int e = 0; e < V; ++e) {
+              const int gi = (wr0 + row) * V + e;
+              if (gi < g0 || gi >= g0 + ng) continue;
+              uint32_t zp[4];
+#pragma unroll
+              for (int q = 0; q < 4; ++q)
+                zp[q] = ((Magic<BF16>::kPair & 0xFFFFu) + ((ww[q] >> (e * W)) & ((1u << W) - 1u))) * 0x00010001u;
+              *reinterpret_cast<uint4 *>(zw + (gi - g0) * CC + c) = make_uint4(zp[0], zp[1], zp[2], zp[3]);
+            }
+          }
+        }
       }
     }
     consumer_sync();
@@ -376,12 +414,20 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_min_blocks(MT, TN))
       const int m = q / qpr, col = (q % qpr) * 4;
       const uint32_t la = red + (m * RP + col) * 4;
       float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int r = 0; r < p.splits; ++r) {
-        const float4 u = ld_dsmem_f4(dsmem_addr(la, (uint32_t)r));
-        v.x += u.x;
-        v.y += u.y;
-        v.z += u.z;
-        v.w += u.w;
+      // up to eight remote loads in flight before the adds (still in split order)
+      for (int r0 = 0; r0 < p.splits; r0 += 8) {
+        float4 u[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if (r0 + j < p.splits) u[j] = ld_dsmem_f4(dsmem_addr(la, (uint32_t)(r0 + j)));
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if (r0 + j < p.splits) {
+            v.x += u[j].x;
+            v.y += u[j].y;
+            v.z += u[j].z;
+            v.w += u[j].w;
+          }
       }
       if (W == 8) {
         const float4 s4 = __ldg(reinterpret_cast<const float4 *>(sc32 + n0 + col));
