@@ -2,6 +2,10 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <map>
+#include <mutex>
+#include <tuple>
+
 #include "decode.cuh"
 
 namespace wq {
@@ -73,6 +77,40 @@ static void rows_for(int K, int kc, int gs, int cps, int V, int *srows, int *zro
   *zrows = zr;
 }
 
+// Resident-CTA capacity of one launch shape (decode_capacity_t), asked once
+// per device and shape.  Clusters of up to kMaxClusterSplits CTAs carry the
+// K splits; more splits run as independent CTAs.
+static long capacity(int w_bit, int fold, int mt, int tn, bool zero, int smem, int splits, int sms) {
+  const int cs = (splits > 1 && splits <= kMaxClusterSplits) ? splits : 1;
+  const bool z = zero && w_bit != 8;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  using Key = std::tuple<int, int, int, int, int, bool, int, int>;
+  static std::map<Key, long> cache;
+  static std::mutex mu;
+  const Key key{dev, w_bit, fold, mt, tn, z, smem, cs};
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+  }
+  long c = -1;
+  switch (w_bit * 16 + fold) {
+    case 2 * 16 + 0: c = decode_capacity_wf<2, 0>(mt, tn, z, smem, cs, sms); break;
+    case 2 * 16 + 2: c = decode_capacity_wf<2, 2>(mt, tn, z, smem, cs, sms); break;
+    case 2 * 16 + 4: c = decode_capacity_wf<2, 4>(mt, tn, z, smem, cs, sms); break;
+    case 2 * 16 - 1: c = decode_capacity_wf<2, -1>(mt, tn, z, smem, cs, sms); break;
+    case 4 * 16 + 0: c = decode_capacity_wf<4, 0>(mt, tn, z, smem, cs, sms); break;
+    case 4 * 16 + 2: c = decode_capacity_wf<4, 2>(mt, tn, z, smem, cs, sms); break;
+    case 4 * 16 - 1: c = decode_capacity_wf<4, -1>(mt, tn, z, smem, cs, sms); break;
+    case 8 * 16 + 0: c = decode_capacity_wf<8, 0>(mt, tn, z, smem, cs, sms); break;
+  }
+  cudaGetLastError();  // a failed query leaves no error behind for the next launch
+  std::lock_guard<std::mutex> lock(mu);
+  cache[key] = c;
+  return c;
+}
+
 DecodePlan plan_decode(int M, int N, int K, int w_bit, int group_size, bool zero, int sms) {
   DecodePlan best{};
   const int rows = M < 64 ? M : 64;
@@ -83,54 +121,61 @@ DecodePlan plan_decode(int M, int N, int K, int w_bit, int group_size, bool zero
   const int gs = (w_bit == 8 || group_size <= 0) ? K : group_size;
   const bool grouped = w_bit != 8;
   const int V = 32 / w_bit;
-  // Tile columns per warp: two (the CTA covers 128 channels) keep three CTAs
-  // of four consumer warps on an SM; int2 codes with one token tile take four
-  // (their long chunk rows make the activation loads per tile the larger cost).
-  // 64-row slices use one.
-  int tns[1] = {w_bit == 2 && mt == 1 ? 4 : 2};
-  const int ntn = 1;
-  if (mt == 8) tns[0] = 1;
+  // Two 16-channel tiles per warp (the CTA covers 128 channels) keep three
+  // CTAs of four consumer warps on an SM; 64-row slices take one.
+  const int tn = mt == 8 ? 1 : 2;
+  const int nblocks = (nt + kDecodeWarps * tn - 1) / (kDecodeWarps * tn);
+  const double unit_bytes = (double)tn * kDecodeWarps * 512.0;  // one chunk row of a CTA
+  const int fold = fold_for(w_bit, gs);
   double best_cost = 1e300;
-  for (int a = 0; a < ntn; ++a) {
-    const int tn = tns[a];
-    const int nblocks = (nt + kDecodeWarps * tn - 1) / (kDecodeWarps * tn);
-    const int smax = kch < 256 ? kch : 256;
-    for (int s = 1; s <= smax; ++s) {
-      const int cps = (kch + s - 1) / s;
-      const int sreal = (kch + cps - 1) / cps;
-      if (s != sreal) continue;
-      int srows = 0, zrows = 0;
-      if (grouped) rows_for(K, kc, gs, cps, V, &srows, &zrows);
-      zrows = zero ? srows : 0;  // one (MAGIC + zero) row per group
-      const int smem = DecodeSmem{w_bit, mt, tn, srows, zrows}.bytes();
-      if (smem > 200 * 1024) continue;
-      int occ = decode_min_blocks(mt, tn);  // the register budget the kernel is compiled for
+  const int smax = kch < 256 ? kch : 256;
+  for (int s = 1; s <= smax; ++s) {
+    const int cps = (kch + s - 1) / s;
+    const int sreal = (kch + cps - 1) / cps;
+    if (s != sreal) continue;
+    int srows = 0, zrows = 0;
+    if (grouped) rows_for(K, kc, gs, cps, V, &srows, &zrows);
+    zrows = zero ? srows : 0;  // one (MAGIC + zero) row per group
+    const int smem = DecodeSmem{w_bit, mt, tn, srows, zrows}.bytes();
+    if (smem > 200 * 1024) continue;
+    long cap = capacity(w_bit, fold, mt, tn, zero, smem, sreal, sms);
+    if (cap < 0) {  // no answer from the runtime: the register budget the kernel is compiled for
+      int occ = decode_min_blocks(mt, tn);
       const int by_smem = (228 * 1024) / (smem + 1024);
-      occ = occ < by_smem ? occ : by_smem;
-      if (occ < 1) continue;
-      const long slots = (long)sms * occ;
-      const long units = (long)nblocks * sreal;
-      // weight bytes the busiest SM streams (one wave if the units fit the slots)
-      const long per_sm = units <= slots ? (units + sms - 1) / sms : ((units + slots - 1) / slots) * occ;
-      double cost = (double)per_sm * (cps * (double)tn * kDecodeWarps * 512.0 + 8192.0);
-      // split-K: reduction in the cluster's shared memory (up to 16 splits), or
-      // the partial sums' round trip through the workspace
-      if (sreal > 1 && sreal <= kMaxClusterSplits) cost += 2.0 * rows * (double)N * sreal / sms;
-      if (sreal > kMaxClusterSplits) cost += 8.0 * rows * (double)N * sreal / sms;
-      if (cost < best_cost * 0.999) {
-        best_cost = cost;
-        best.mt = mt;
-        best.tn = tn;
-        best.nblocks = nblocks;
-        best.splits = sreal;
-        best.cps = cps;
-        best.srows = srows;
-        best.zrows = zrows;
-        best.smem = smem;
-      }
+      cap = (long)sms * (occ < by_smem ? occ : by_smem);
+    }
+    if (cap < 1) continue;
+    // Estimated time in microseconds.  The busiest SM streams per_sm CTAs'
+    // chunk rows; an SM's rate grows with the CTAs it runs at once (r), as
+    // their warps hide each other's latency (rate r / (r + 3) of about
+    // 60 KB/us, fitted to measured decode launches).  Each wave then pays the
+    // K-split reduction: a cluster's barriers and remote loads cost about
+    // 0.3 us + 0.5 us per split, plus a round trip per eight splits beyond
+    // the first eight; through the workspace the last CTA of a column block
+    // adds the partials, its threads taking a round trip of about 1 us per
+    // eight splits for every 128 quads of outputs.
+    const long units = (long)nblocks * sreal;
+    const long waves = (units + cap - 1) / cap;
+    const long per_sm_max = (cap + sms - 1) / sms;
+    const long per_sm = units <= cap ? (units + sms - 1) / sms : waves * per_sm_max;
+    const double r = (double)(per_sm < per_sm_max ? per_sm : per_sm_max);
+    double cost = (double)per_sm * cps * unit_bytes / (60e3 * r / (r + 3.0));
+    if (sreal == 1) cost += 0.3 * waves;
+    else if (sreal <= kMaxClusterSplits) cost += (0.3 + 0.5 * sreal + 1.0 * ((sreal + 7) / 8 - 1)) * waves;
+    else cost += (2.0 + 1.0 * ((rows * kDecodeWarps * tn * 4 + 127) / 128) * ((sreal + 7) / 8)) * waves;
+    if (cost < best_cost * 0.999) {
+      best_cost = cost;
+      best.mt = mt;
+      best.tn = tn;
+      best.nblocks = nblocks;
+      best.splits = sreal;
+      best.cps = cps;
+      best.srows = srows;
+      best.zrows = zrows;
+      best.smem = smem;
     }
   }
-  best.fold = fold_for(w_bit, gs);
+  best.fold = fold;
   best.cluster = best.splits > 1 && best.splits <= kMaxClusterSplits;
   best.workspace = best.splits > kMaxClusterSplits
                        ? decode_counter_bytes() + (size_t)best.splits * rows * N * sizeof(float)

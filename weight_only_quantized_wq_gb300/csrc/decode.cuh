@@ -499,18 +499,35 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_min_blocks(MT, TN))
   if (threadIdx.x == 0) p.counters[nb] = 0;
 }
 
+// Kernel attributes a launch (or an occupancy query) of `smem` dynamic
+// shared memory and clusters of more than eight CTAs needs, set once per
+// device and size.
 template <int W, bool BF16, int MT, int TN, bool ZERO, int FOLD>
-cudaError_t launch_decode_t(const DecodeParams &dp, const DecodePlan &p, cudaStream_t s) {
+cudaError_t prepare_decode_t(int smem, bool big_cluster) {
   auto kern = decode_kernel<W, BF16, MT, TN, ZERO, FOLD>;
-  const int smem = p.smem;
   static int attr_bytes[64] = {0};
+  static bool nonportable[64] = {false};
   int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && attr_bytes[dev] < smem) {
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (attr_bytes[dev] < smem) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     attr_bytes[dev] = smem;
   }
+  if (big_cluster && !nonportable[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+    nonportable[dev] = true;
+  }
+  return cudaSuccess;
+}
+
+template <int W, bool BF16, int MT, int TN, bool ZERO, int FOLD>
+cudaError_t launch_decode_t(const DecodeParams &dp, const DecodePlan &p, cudaStream_t s) {
+  auto kern = decode_kernel<W, BF16, MT, TN, ZERO, FOLD>;
+  const int smem = p.smem;
+  cudaError_t e = prepare_decode_t<W, BF16, MT, TN, ZERO, FOLD>(smem, dp.cluster && p.splits > 8);
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(p.nblocks, p.splits);
   cfg.blockDim = dim3(kDecodeThreads);
@@ -518,10 +535,6 @@ cudaError_t launch_decode_t(const DecodeParams &dp, const DecodePlan &p, cudaStr
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   if (dp.cluster) {
-    if (p.splits > 8) {
-      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-      if (e != cudaSuccess) return e;
-    }
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 1;
     attr[0].val.clusterDim.y = p.splits;
@@ -529,8 +542,38 @@ cudaError_t launch_decode_t(const DecodeParams &dp, const DecodePlan &p, cudaStr
     cfg.attrs = attr;
     cfg.numAttrs = 1;
   }
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, dp);
+  e = cudaLaunchKernelEx(&cfg, kern, dp);
   return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+// CTAs of one launch that can be resident at once, from the runtime's
+// occupancy calculator: CTAs per SM x SMs, and for a cluster launch of
+// `splits` CTAs the clusters the GPCs can hold x splits.  -1 on error.
+template <int W, bool BF16, int MT, int TN, bool ZERO, int FOLD>
+long decode_capacity_t(int smem, int splits, int sms) {
+  auto kern = decode_kernel<W, BF16, MT, TN, ZERO, FOLD>;
+  const bool cluster = splits > 1 && splits <= kMaxClusterSplits;
+  if (prepare_decode_t<W, BF16, MT, TN, ZERO, FOLD>(smem, cluster && splits > 8) != cudaSuccess) return -1;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kDecodeThreads, smem) != cudaSuccess) return -1;
+  long cap = (long)per_sm * sms;
+  if (cluster) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(1, splits);
+    cfg.blockDim = dim3(kDecodeThreads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = splits;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int nc = 0;
+    if (cudaOccupancyMaxActiveClusters(&nc, kern, &cfg) != cudaSuccess) return -1;
+    cap = cap < (long)nc * splits ? cap : (long)nc * splits;
+  }
+  return cap;
 }
 
 // Launcher for one code width and group schedule (decode_inst.cu, compiled
@@ -538,8 +581,16 @@ cudaError_t launch_decode_t(const DecodeParams &dp, const DecodePlan &p, cudaStr
 template <int W, int FOLD>
 cudaError_t launch_decode_wf(const DecodeParams &dp, const DecodePlan &p, bool bf16, bool zero, cudaStream_t s);
 
+template <int W, int FOLD>
+long decode_capacity_wf(int mt, int tn, bool zero, int smem, int splits, int sms);
+
 #define WQ_DECODE_CASE(W, BF, MT, TN, Z, F)                               \
   if (bf16 == BF && zero == Z && p.mt == MT && p.tn == TN && p.fold == F) \
     return launch_decode_t<W, BF, MT, TN, Z, F>(dp, p, s);
+
+// The capacity of the bf16 instantiation stands for both activation types
+// (the plan, and so the workspace size, must not depend on the x dtype).
+#define WQ_DECODE_CAPACITY(W, MT, TN, Z, F) \
+  if (zero == Z && mt == MT && tn == TN) return decode_capacity_t<W, true, MT, TN, Z, F>(smem, splits, sms);
 
 }  // namespace wq

@@ -13,7 +13,6 @@ template <>
 cudaError_t launch_decode_wf<WQ_W, WQ_FOLD>(const DecodeParams &dp, const DecodePlan &p, bool bf16, bool zero,
                                             cudaStream_t s) {
 #define SHAPES(BF, Z)                       \
-  WQ_DECODE_CASE(WQ_W, BF, 1, 4, Z, WQ_FOLD) \
   WQ_DECODE_CASE(WQ_W, BF, 1, 2, Z, WQ_FOLD) \
   WQ_DECODE_CASE(WQ_W, BF, 2, 2, Z, WQ_FOLD) \
   WQ_DECODE_CASE(WQ_W, BF, 4, 2, Z, WQ_FOLD) \
@@ -29,6 +28,23 @@ cudaError_t launch_decode_wf<WQ_W, WQ_FOLD>(const DecodeParams &dp, const Decode
 #endif
 #undef SHAPES
   return cudaErrorInvalidValue;
+}
+
+template <>
+long decode_capacity_wf<WQ_W, WQ_FOLD>(int mt, int tn, bool zero, int smem, int splits, int sms) {
+#define SHAPES(Z)                            \
+  WQ_DECODE_CAPACITY(WQ_W, 1, 2, Z, WQ_FOLD) \
+  WQ_DECODE_CAPACITY(WQ_W, 2, 2, Z, WQ_FOLD) \
+  WQ_DECODE_CAPACITY(WQ_W, 4, 2, Z, WQ_FOLD) \
+  WQ_DECODE_CAPACITY(WQ_W, 8, 1, Z, WQ_FOLD)
+#if WQ_W == 8
+  SHAPES(false)
+#else
+  SHAPES(true)
+  SHAPES(false)
+#endif
+#undef SHAPES
+  return -1;
 }
 
 }  // namespace wq
