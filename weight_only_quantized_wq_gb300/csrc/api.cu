@@ -136,8 +136,10 @@ size_t wq_workspace_bytes(int M, int N, int K, int w_bit, int group_size) {
   if (device_info(&d) != WQ_OK) return 0;
   if (w_bit == 8 || group_size == -1) group_size = K;
   if (group_size <= 0 || K % group_size != 0) return 0;
-  // The split (and so the workspace) does not depend on the zeros.
-  return slice_workspace(M, N, K, w_bit, group_size, true, d->sms);
+  // Enough with zeros or without (the zero rows' shared memory can change the split).
+  const size_t with_z = slice_workspace(M, N, K, w_bit, group_size, true, d->sms);
+  const size_t without = w_bit == 8 ? with_z : slice_workspace(M, N, K, w_bit, group_size, false, d->sms);
+  return with_z > without ? with_z : without;
 }
 
 wq_status wq_matmul(const void *x, wq_dtype x_dtype, const void *packed_w, const void *scales, wq_dtype s_dtype,

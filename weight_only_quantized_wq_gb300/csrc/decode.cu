@@ -29,17 +29,18 @@ static EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// Row-major 2-D 16-bit tensor (rows x cols) and a box of (box_cols x box_rows),
-// no swizzle, zero fill outside the tensor.
+// Row-major 2-D tensor of 16- or 32-bit elements (rows x cols) and a box of
+// (box_cols x box_rows), no swizzle, zero fill outside the tensor.
 static bool encode_2d(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows, uint32_t box_cols,
-                      uint32_t box_rows) {
+                      uint32_t box_rows, int elem_bytes = 2) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[2] = {cols, rows};
-  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint64_t strides[1] = {cols * (uint64_t)elem_bytes};
   const cuuint32_t box[2] = {box_cols, box_rows};
   const cuuint32_t estr[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+  const CUtensorMapDataType dt = elem_bytes == 4 ? CU_TENSOR_MAP_DATA_TYPE_UINT32 : CU_TENSOR_MAP_DATA_TYPE_UINT16;
+  return fn(m, dt, 2, const_cast<void *>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -133,10 +134,12 @@ DecodePlan plan_decode(int M, int N, int K, int w_bit, int group_size, bool zero
     const int cps = (kch + s - 1) / s;
     const int sreal = (kch + cps - 1) / cps;
     if (s != sreal) continue;
-    int srows = 0, zrows = 0;
-    if (grouped) rows_for(K, kc, gs, cps, V, &srows, &zrows);
-    zrows = zero ? srows : 0;  // one (MAGIC + zero) row per group
-    const int smem = DecodeSmem{w_bit, mt, tn, srows, zrows}.bytes();
+    int srows = 0, zwrows = 0;
+    if (grouped) rows_for(K, kc, gs, cps, V, &srows, &zwrows);
+    if (!zero) zwrows = 0;
+    const int zrows = zero ? srows : 0;  // one (MAGIC + zero) row per group
+    if (srows > 256 || zwrows > 256) continue;  // one TMA box each
+    const int smem = DecodeSmem{w_bit, mt, tn, srows, zrows, zwrows}.bytes();
     if (smem > 200 * 1024) continue;
     long cap = capacity(w_bit, fold, mt, tn, zero, smem, sreal, sms);
     if (cap < 0) {  // no answer from the runtime: the register budget the kernel is compiled for
@@ -172,6 +175,7 @@ DecodePlan plan_decode(int M, int N, int K, int w_bit, int group_size, bool zero
       best.cps = cps;
       best.srows = srows;
       best.zrows = zrows;
+      best.zwrows = zwrows;
       best.smem = smem;
     }
   }
@@ -200,6 +204,7 @@ cudaError_t launch_decode(const MatmulArgs &a, const DecodePlan &p, void *worksp
   dp.cps = p.cps;
   dp.srows = p.srows;
   dp.zrows = p.zrows;
+  dp.zwrows = p.zwrows;
   dp.s_bf16 = a.s_bf16;
   dp.cluster = p.cluster;
   if (p.splits > 1 && !p.cluster) {
@@ -209,6 +214,15 @@ cudaError_t launch_decode(const MatmulArgs &a, const DecodePlan &p, void *worksp
   // Tensor map of the activation slice of a stage (rows past M read as zeros).
   if (!encode_2d(&dp.tm_x, a.x, (uint64_t)a.K, (uint64_t)a.M, (uint32_t)(x_pitch(a.w_bit) / 2), (uint32_t)(p.mt * 8)))
     return cudaErrorInvalidValue;
+  // Scale rows and zero-word rows of a CTA: one box of (CTA columns x rows) each.
+  const uint32_t cols = (uint32_t)(kDecodeWarps * p.tn * 16);
+  if (a.w_bit != 8) {
+    const int G = a.K / a.group_size, V = 32 / a.w_bit;
+    if (!encode_2d(&dp.tm_s, a.scales, (uint64_t)a.N, (uint64_t)G, cols, (uint32_t)p.srows))
+      return cudaErrorInvalidValue;
+    if (a.zeros && !encode_2d(&dp.tm_z, a.zeros, (uint64_t)a.N, (uint64_t)((G + V - 1) / V), cols, (uint32_t)p.zwrows, 4))
+      return cudaErrorInvalidValue;
+  }
   const bool z = a.zeros != nullptr;
   const bool bf = a.x_bf16;
   switch (a.w_bit * 16 + p.fold) {

@@ -66,16 +66,19 @@ __host__ __device__ constexpr int align128(int v) { return (v + 127) / 128 * 128
 // is 8 mod 32, which makes the 8-byte B-fragment loads of a warp conflict-free.
 __host__ __device__ constexpr int x_pitch(int w) { return 4 * ((128 / w) + ((8 - (128 / w) % 32) + 32) % 32); }
 
-// Shared-memory layout of one CTA: barriers | staged scales (fp32, one row per
-// group) | staged (MAGIC + zero) pairs (one row per group, asymmetric codes
-// only: zrows = srows, else 0) | ring of stages (packed weights, then the
-// activation slice).
+// Shared-memory layout of one CTA: barriers | scales as stored (16-bit, one
+// row per group) | (MAGIC + zero) pairs (one row per group, asymmetric codes
+// only: zrows = srows, else 0) | packed zero words as stored (zwrows rows) |
+// ring of stages (packed weights, then the activation slice).  The scale and
+// zero-word rows arrive by TMA, one box each, so srows and zwrows are at most
+// 256.
 struct DecodeSmem {
-  int w, mt, tn, srows, zrows;
+  int w, mt, tn, srows, zrows, zwrows;
   __host__ __device__ constexpr int cols() const { return kDecodeWarps * tn * 16; }
   __host__ __device__ constexpr int s_off() const { return kDecodeHeader; }
-  __host__ __device__ constexpr int z_off() const { return align128(s_off() + srows * cols() * 4); }
-  __host__ __device__ constexpr int ring_off() const { return align128(z_off() + zrows * cols() * 4); }
+  __host__ __device__ constexpr int z_off() const { return align128(s_off() + srows * cols() * 2); }
+  __host__ __device__ constexpr int zw_off() const { return align128(z_off() + zrows * cols() * 4); }
+  __host__ __device__ constexpr int ring_off() const { return align128(zw_off() + zwrows * cols() * 4); }
   __host__ __device__ constexpr int w_bytes() const { return cols() * 32; }  // one chunk row of weights
   __host__ __device__ constexpr int x_off() const { return w_bytes(); }
   __host__ __device__ constexpr int x_bytes() const { return mt * 8 * x_pitch(w); }
@@ -85,6 +88,8 @@ struct DecodeSmem {
 
 struct DecodeParams {
   CUtensorMap tm_x;  // x (M, K) 16-bit; box (x_pitch/2, 8*MT): the row pitch padding is real data or zeros
+  CUtensorMap tm_s;  // scales (G, N) 16-bit; box (CTA columns, srows)       [grouped codes]
+  CUtensorMap tm_z;  // zero words (ceil(G/V), N) 32-bit; box (CTA columns, zwrows) [asymmetric]
   const uint8_t *packed;
   const void *scales;     // (G, N) 16-bit, or (N,) fp32 for int8
   const uint32_t *zeros;  // (ceil(G / V), N) or nullptr
@@ -92,7 +97,7 @@ struct DecodeParams {
   float *partial;
   int *counters;
   uint32_t *err;
-  int M, N, K, gs, nt_total, kch, splits, cps, srows, zrows;
+  int M, N, K, gs, nt_total, kch, splits, cps, srows, zrows, zwrows;
   bool s_bf16;
   bool cluster;  // the splits of a column block form a cluster (reduction in shared memory)
 };
@@ -120,11 +125,12 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_min_blocks(MT, TN))
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ int s_last;
   __shared__ volatile int s_abort;
-  const DecodeSmem L{W, MT, TN, p.srows, p.zrows};
+  const DecodeSmem L{W, MT, TN, p.srows, p.zrows, p.zwrows};
   uint64_t *full = reinterpret_cast<uint64_t *>(smem);
   uint64_t *empty = full + STAGES;
-  static_assert(2 * STAGES * 8 <= kDecodeHeader, "barriers do not fit the header");
-  const float *s_sm = reinterpret_cast<const float *>(smem + L.s_off());         // [srows][CC] scales
+  uint64_t *meta = empty + STAGES;  // the scale and zero-word rows have landed
+  static_assert((2 * STAGES + 1) * 8 <= kDecodeHeader, "barriers do not fit the header");
+  const uint16_t *s_sm = reinterpret_cast<const uint16_t *>(smem + L.s_off());  // [srows][CC] scales
   const uint32_t *z_sm = reinterpret_cast<const uint32_t *>(smem + L.z_off());  // [zrows][CC] MAGIC + zero pairs
   uint8_t *ring = smem + L.ring_off();
   const int SB = L.stage_bytes();
@@ -143,6 +149,7 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_min_blocks(MT, TN))
       mbar_init(smem_addr(&full[i]), 1);
       mbar_init(smem_addr(&empty[i]), NW * 32);  // every consumer lane arrives
     }
+    mbar_init(smem_addr(meta), 1);
     s_abort = 0;
     fence_barrier_init();
   }
@@ -154,6 +161,13 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_min_blocks(MT, TN))
     const uint32_t wbytes = (uint32_t)ntiles * 512u;
     const uint32_t xbytes = (uint32_t)L.x_bytes();
     int issued = 0;
+    const int g0 = GROUPED ? kbeg / p.gs : 0;
+    if (GROUPED && lane == 0) {  // this CTA's scale rows (and zero-word rows) ahead of the ring
+      const uint32_t mb = smem_addr(meta);
+      mbar_arrive_expect_tx(mb, (uint32_t)(L.srows * CC * 2 + L.zwrows * CC * 4));
+      tma_load_2d(smem_addr(smem + L.s_off()), &p.tm_s, n0, g0, mb);
+      if (ZERO) tma_load_2d(smem_addr(smem + L.zw_off()), &p.tm_z, n0, g0 / V, mb);
+    }
     if (lane == 0) {
       int st = 0;
       uint32_t ph = 0;  // phase parity of the ring's current lap
@@ -174,6 +188,7 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_min_blocks(MT, TN))
       // No copy may still be writing this CTA's shared memory when it exits.
       for (int i = max(0, issued - STAGES); i < issued; ++i)
         mbar_wait(smem_addr(&full[i % STAGES]), (i / STAGES) & 1, p.err, nullptr);
+      if (GROUPED) mbar_wait(smem_addr(meta), 0, p.err, nullptr);
     }
     __syncwarp();
     if (p.cluster) {  // the consumers' two cluster barriers
@@ -187,77 +202,27 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_min_blocks(MT, TN))
   const int g = lane >> 2, t = lane & 3;
   const int wt0 = warp * TN;  // first tile of this warp within the CTA
 
-  // Scales (as fp32) and (MAGIC + zero) pairs of the CTA's groups -> shared
-  // memory, while the producer fills the ring.
+  // The scale rows stay as stored (16-bit, converted when a group is
+  // folded); the packed zero words become one (MAGIC + zero) pair per group
+  // and column, built once per CTA.
   const int g0 = GROUPED ? kbeg / p.gs : 0;
   if constexpr (GROUPED) {
-    constexpr int CT = NW * 32;  // consumer threads
-    constexpr int SB4 = 4;       // loads in flight per thread
-    const int ng = (kend - 1) / p.gs - g0 + 1;
-    const int cols = ntiles * 16;
-    float *sw = reinterpret_cast<float *>(smem + L.s_off());
-    const uint16_t *sg = static_cast<const uint16_t *>(p.scales);
-    const int sitems = ng * (cols / 8);  // 8 scales per 16-byte load
-    for (int b0 = 0; b0 < sitems; b0 += SB4 * CT) {
-      uint4 h[SB4];
+    const bool ok = mbar_wait(smem_addr(meta), 0, p.err, &s_abort);
+    if (ZERO && ok) {
+      const int ng = (kend - 1) / p.gs - g0 + 1;
+      const int wr0 = g0 / V;
+      const uint32_t *zw = reinterpret_cast<const uint32_t *>(smem + L.zw_off());
+      uint32_t *zz_out = reinterpret_cast<uint32_t *>(smem + L.z_off());
+      for (int idx = threadIdx.x; idx < ng * (CC / 4); idx += NW * 32) {
+        const int row = idx / (CC / 4), c = (idx % (CC / 4)) * 4;
+        const int gi = g0 + row, sh = (gi % V) * W;
+        const uint4 w4 = *reinterpret_cast<const uint4 *>(zw + (gi / V - wr0) * CC + c);
+        const uint32_t ww[4] = {w4.x, w4.y, w4.z, w4.w};
+        uint32_t zp[4];
 #pragma unroll
-      for (int j = 0; j < SB4; ++j) {
-        const int idx = b0 + j * CT + threadIdx.x;
-        if (idx < sitems) {
-          const int row = idx / (cols / 8), c = (idx % (cols / 8)) * 8;
-          h[j] = ldg_nc128(sg + (size_t)(g0 + row) * p.N + n0 + c);
-        }
-      }
-#pragma unroll
-      for (int j = 0; j < SB4; ++j) {
-        const int idx = b0 + j * CT + threadIdx.x;
-        if (idx < sitems) {
-          const int row = idx / (cols / 8), c = (idx % (cols / 8)) * 8;
-          const uint32_t hw[4] = {h[j].x, h[j].y, h[j].z, h[j].w};
-          float f[8];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            f[2 * e] = half_bits_to_float((uint16_t)(hw[e] & 0xFFFFu), p.s_bf16);
-            f[2 * e + 1] = half_bits_to_float((uint16_t)(hw[e] >> 16), p.s_bf16);
-          }
-          *reinterpret_cast<float4 *>(sw + row * CC + c) = make_float4(f[0], f[1], f[2], f[3]);
-          *reinterpret_cast<float4 *>(sw + row * CC + c + 4) = make_float4(f[4], f[5], f[6], f[7]);
-        }
-      }
-    }
-    if constexpr (ZERO) {
-      // Each packed zero word holds V groups: read every word row once and
-      // write the (MAGIC + zero) pairs of the groups of this CTA it holds.
-      uint32_t *zw = reinterpret_cast<uint32_t *>(smem + L.z_off());
-      const int wr0 = g0 / V, nwr = (g0 + ng - 1) / V - wr0 + 1;
-      const int zitems = nwr * (cols / 4);  // 4 words per 16-byte load
-      for (int b0 = 0; b0 < zitems; b0 += SB4 * CT) {
-        uint4 w4[SB4];
-#pragma unroll
-        for (int j = 0; j < SB4; ++j) {
-          const int idx = b0 + j * CT + threadIdx.x;
-          if (idx < zitems) {
-            const int row = idx / (cols / 4), c = (idx % (cols / 4)) * 4;
-            w4[j] = ldg_nc128(p.zeros + (size_t)(wr0 + row) * p.N + n0 + c);
-          }
-        }
-#pragma unroll
-        for (int j = 0; j < SB4; ++j) {
-          const int idx = b0 + j * CT + threadIdx.x;
-          if (idx < zitems) {
-            const int row = idx / (cols / 4), c = (idx % (cols / 4)) * 4;
-            const uint32_t ww[4] = {w4[j].x, w4[j].y, w4[j].z, w4[j].w};
-            for (int e = 0; e < V; ++e) {
-              const int gi = (wr0 + row) * V + e;
-              if (gi < g0 || gi >= g0 + ng) continue;
-              uint32_t zp[4];
-#pragma unroll
-              for (int q = 0; q < 4; ++q)
-                zp[q] = ((Magic<BF16>::kPair & 0xFFFFu) + ((ww[q] >> (e * W)) & ((1u << W) - 1u))) * 0x00010001u;
-              *reinterpret_cast<uint4 *>(zw + (gi - g0) * CC + c) = make_uint4(zp[0], zp[1], zp[2], zp[3]);
-            }
-          }
-        }
+        for (int e = 0; e < 4; ++e)
+          zp[e] = ((Magic<BF16>::kPair & 0xFFFFu) + ((ww[e] >> sh) & ((1u << W) - 1u))) * 0x00010001u;
+        *reinterpret_cast<uint4 *>(zz_out + row * CC + c) = make_uint4(zp[0], zp[1], zp[2], zp[3]);
       }
     }
     consumer_sync();
@@ -295,7 +260,7 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_min_blocks(MT, TN))
     for (int ti = 0; ti < TN; ++ti)
 #pragma unroll
       for (int rr = 0; rr < 2; ++rr) {
-        const float s = s_sm[(gi - g0) * CC + (wt0 + ti) * 16 + g + 8 * rr];
+        const float s = half_bits_to_float(s_sm[(gi - g0) * CC + (wt0 + ti) * 16 + g + 8 * rr], p.s_bf16);
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt)
 #pragma unroll

@@ -24,8 +24,9 @@ struct MatmulArgs {
 
 // Split of a few-token kernel over the GPU, chosen on the host.
 struct DecodePlan {
-  int srows;     // scale rows one CTA stages in shared memory
-  int zrows;     // zero-word rows one CTA stages in shared memory
+  int srows;     // scale rows (groups) one CTA stages in shared memory
+  int zrows;     // (MAGIC + zero) rows one CTA builds (srows for asymmetric codes, else 0)
+  int zwrows;    // packed zero-word rows one CTA copies in (0 for symmetric codes)
   int smem;      // dynamic shared memory bytes
   int mt;        // 8-row token tiles (1, 2, 4, 8)
   int tn;        // 16-row weight tiles per warp
