@@ -49,6 +49,19 @@ def test_prefill_sweep_sampled_rows(M):
     assert np.all(np.isfinite(y))
 
 
+@pytest.mark.parametrize("M", [24, 32, 48])
+def test_decode_several_waves_sampled_rows(M):
+    # 32- and 64-row token tiles on the c5 weights: more CTAs (clusters of K
+    # splits) than the GPU holds at once, so clusters start as others retire.
+    full, d = _sweep()
+    p = full.rows(M)
+    dd = dict(d, x=d["x"][:M].contiguous())
+    for _ in range(2):
+        y = run(p, dd).cpu().numpy()
+        rows = [0, M // 3, M // 2 + 1, M - 1]
+        assert_close(y[rows], oracle_y(p, rows=rows), p.K, p.name)
+
+
 INT_EXACT = [  # (name, M, K, N, w_bit, group, x, s, symmetric)
     ("int4-asym-f16", 1, 512, 512, 4, 128, "f16", "f16", False),
     ("int4-sym-f16", 3, 4096, 1024, 4, 128, "f16", "f16", True),
