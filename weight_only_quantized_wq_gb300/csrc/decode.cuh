@@ -193,7 +193,7 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_min_blocks(MT, TN))
     __syncwarp();
     if (p.cluster) {  // the consumers' two cluster barriers
       cluster_sync();
-      cluster_sync();
+      cluster_sync_relaxed();
     }
     return;
   }
@@ -403,7 +403,8 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_min_blocks(MT, TN))
       }
       *reinterpret_cast<float4 *>(p.out + (size_t)m * p.N + n0 + col) = v;
     }
-    cluster_sync();  // no CTA leaves while another still reads its shared memory
+    __syncwarp();
+    cluster_sync_relaxed();  // no CTA leaves while another still reads its shared memory
     return;
   }
   float *dst = p.splits == 1 ? p.out : p.partial + (size_t)split * p.M * p.N;
