@@ -114,6 +114,9 @@ WQ_API wq_status wq_unpack(const void *packed, int K, int N, int w_bit, uint8_t 
  * counters at zero again, so one zero-fill at allocation is enough for any
  * later call, whatever its shape, as long as the buffer is large enough.  Calls that share a workspace must not
  * run concurrently (they would race on the counters and partials).
+ * The split along K (and so this size) is chosen with the runtime's occupancy
+ * calculator for the current device; the answer covers both the asymmetric
+ * (zeros given) and the symmetric case.
  */
 WQ_API size_t wq_workspace_bytes(int M, int N, int K, int w_bit, int group_size);
 
@@ -140,6 +143,9 @@ WQ_API size_t wq_workspace_bytes(int M, int N, int K, int w_bit, int group_size)
  * Precision: the weight codes and zeros enter the tensor cores exactly; the
  * group scale and zero are applied to the fp32 partial sum of each group (small
  * M) or to the weight, rounded once to the x dtype (large M).
+ * The first call for a problem shape on a device asks the runtime's occupancy
+ * calculator (host-side queries, cached per device and shape) and sets kernel
+ * attributes; make that first call outside stream capture.
  */
 WQ_API wq_status wq_matmul(const void *x, wq_dtype x_dtype, const void *packed_w,
                     const void *scales, wq_dtype s_dtype, const int32_t *zeros,
