@@ -55,8 +55,11 @@ namespace wq {
 constexpr int kDecodeWarps = 4;  // consumer warps per CTA (plus one producer warp)
 constexpr int kDecodeThreads = (kDecodeWarps + 1) * 32;
 constexpr int kDecodeHeader = 256;  // mbarriers in front of the staged rows
-// Ring depth: 24 to 40 KB of weights in flight per CTA.
-__host__ __device__ constexpr int decode_stages(int tn) { return tn >= 4 ? 5 : 6; }
+// Ring depth in chunk rows (slots): 12 to 24 KB of weights in flight per CTA.
+__host__ __device__ constexpr int decode_stages(int) { return 6; }
+// A ring stage holds this many chunk rows (slots): one barrier wait and one
+// release per pair of chunk rows.
+constexpr int kSlotsPerStage = 2;
 // Resident CTAs per SM the register budget is sized for.
 __host__ __device__ constexpr int decode_min_blocks(int mt, int tn) { return mt * tn >= 8 ? 2 : 3; }
 
@@ -69,7 +72,8 @@ __host__ __device__ constexpr int x_pitch(int w) { return 4 * ((128 / w) + ((8 -
 // Shared-memory layout of one CTA: barriers | scales as stored (16-bit, one
 // row per group) | (MAGIC + zero) pairs (one row per group, asymmetric codes
 // only: zrows = srows, else 0) | packed zero words as stored (zwrows rows) |
-// ring of stages (packed weights, then the activation slice).  The scale and
+// ring of stages, each of kSlotsPerStage slots (packed weights of one chunk
+// row, then its activation slice).  The scale and
 // zero-word rows arrive by TMA, one box each, so srows and zwrows are at most
 // 256.
 struct DecodeSmem {
@@ -82,8 +86,9 @@ struct DecodeSmem {
   __host__ __device__ constexpr int w_bytes() const { return cols() * 32; }  // one chunk row of weights
   __host__ __device__ constexpr int x_off() const { return w_bytes(); }
   __host__ __device__ constexpr int x_bytes() const { return mt * 8 * x_pitch(w); }
-  __host__ __device__ constexpr int stage_bytes() const { return align128(x_off() + x_bytes()); }
-  __host__ __device__ constexpr int bytes() const { return ring_off() + decode_stages(tn) * stage_bytes(); }
+  __host__ __device__ constexpr int slot_bytes() const { return align128(x_off() + x_bytes()); }
+  __host__ __device__ constexpr int stage_bytes() const { return kSlotsPerStage * slot_bytes(); }
+  __host__ __device__ constexpr int bytes() const { return ring_off() + decode_stages(tn) * slot_bytes(); }
 };
 
 struct DecodeParams {
@@ -116,7 +121,8 @@ template <int W, bool BF16, int MT, int TN, bool ZERO, int FOLD>
 __global__ void __launch_bounds__(kDecodeThreads, decode_min_blocks(MT, TN))
     decode_kernel(const __grid_constant__ DecodeParams p) {
   using G = Geo<W>;
-  constexpr int NW = kDecodeWarps, STAGES = decode_stages(TN);
+  constexpr int NW = kDecodeWarps, STAGES = decode_stages(TN) / kSlotsPerStage;
+  constexpr int SLOT = DecodeSmem{W, MT, TN, 0, 0, 0}.slot_bytes();
   constexpr int KS = G::KS, KC = G::KC, WK = G::WK, V = G::V;
   constexpr int XP = x_pitch(W);
   constexpr bool GROUPED = (W != 8);
@@ -171,14 +177,18 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_min_blocks(MT, TN))
     if (lane == 0) {
       int st = 0;
       uint32_t ph = 0;  // phase parity of the ring's current lap
-      for (int i = 0; i < nch; ++i) {
+      const int nst = (nch + kSlotsPerStage - 1) / kSlotsPerStage;
+      for (int i = 0; i < nst; ++i) {
         if (i >= STAGES && !mbar_wait(smem_addr(&empty[st]), ph ^ 1u, p.err, &s_abort)) break;
         const uint32_t fb = smem_addr(&full[st]);
         const uint32_t base = smem_addr(ring + st * SB);
-        const int kc = c0 + i;
-        mbar_arrive_expect_tx(fb, wbytes + xbytes);
-        bulk_g2s(base, p.packed + ((size_t)kc * p.nt_total + nt0) * 512, wbytes, fb, pol_w);
-        tma_load_2d(base + L.x_off(), &p.tm_x, kc * KC, 0, fb);
+        const int ns = min(kSlotsPerStage, nch - i * kSlotsPerStage);
+        mbar_arrive_expect_tx(fb, (uint32_t)ns * (wbytes + xbytes));
+        for (int j = 0; j < ns; ++j) {
+          const int kc = c0 + i * kSlotsPerStage + j;
+          bulk_g2s(base + j * SLOT, p.packed + ((size_t)kc * p.nt_total + nt0) * 512, wbytes, fb, pol_w);
+          tma_load_2d(base + j * SLOT + L.x_off(), &p.tm_x, kc * KC, 0, fb);
+        }
         issued = i + 1;
         if (++st == STAGES) {
           st = 0;
@@ -278,70 +288,75 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_min_blocks(MT, TN))
   // A barrier test returns after some latency even when the phase is
   // complete, so a non-blocking test of each stage's barrier is issued one
   // stage early and its answer is only read when that stage starts.
-  bool next_ready = nch > 0 && mbar_test_wait(smem_addr(&full[0]), 0);
-  int st = 0, st1 = 1 % STAGES;  // this stage and the next (ring slots)
+  const int nst = (nch + kSlotsPerStage - 1) / kSlotsPerStage;
+  bool next_ready = nst > 0 && mbar_test_wait(smem_addr(&full[0]), 0);
+  int st = 0, st1 = 1 % STAGES;  // this stage and the next (ring positions)
   uint32_t ph = 0, ph1 = STAGES == 1 ? 1u : 0u;  // their phase parities
-  for (int i = 0; i < nch; ++i) {
+  for (int i = 0; i < nst; ++i) {
     if (!next_ready && !mbar_wait(smem_addr(&full[st]), ph, p.err, &s_abort)) break;
-    if (i + 1 < nch) next_ready = mbar_test_wait(smem_addr(&full[st1]), ph1);
-    const uint32_t base = smem_addr(ring + st * SB);
-    const int kc0 = kbeg + i * KC;
-    uint4 wv[TN];
+    if (i + 1 < nst) next_ready = mbar_test_wait(smem_addr(&full[st1]), ph1);
 #pragma unroll
-    for (int ti = 0; ti < TN; ++ti)
-      wv[ti] = (wt0 + ti) < ntiles ? lds128(base + (wt0 + ti) * 512 + lane * 16) : make_uint4(0, 0, 0, 0);
+    for (int sl = 0; sl < kSlotsPerStage; ++sl) {
+      if (sl > 0 && i * kSlotsPerStage + sl >= nch) break;
+      const uint32_t base = smem_addr(ring + st * SB) + sl * SLOT;
+      const int kc0 = kbeg + (i * kSlotsPerStage + sl) * KC;
+      uint4 wv[TN];
+#pragma unroll
+      for (int ti = 0; ti < TN; ++ti)
+        wv[ti] = (wt0 + ti) < ntiles ? lds128(base + (wt0 + ti) * 512 + lane * 16) : make_uint4(0, 0, 0, 0);
 
 #pragma unroll
-    for (int ks = 0; ks < KS; ++ks) {
-      if constexpr (GROUPED) {
-        const bool maybe = FOLD == 0 ? (ks == 0) : FOLD > 0 ? (ks % (FOLD > 0 ? FOLD : 1) == 0) : true;
-        if (maybe && kc0 + ks * 16 == next_fold) {  // a group ended before this k-step
-          fold(cur_g);
-          ++cur_g;
-          next_fold = min(next_fold + p.gs, kend);
-          set_zeros(cur_g);
+      for (int ks = 0; ks < KS; ++ks) {
+        if constexpr (GROUPED) {
+          const bool maybe = FOLD == 0 ? (ks == 0) : FOLD > 0 ? (ks % (FOLD > 0 ? FOLD : 1) == 0) : true;
+          if (maybe && kc0 + ks * 16 == next_fold) {  // a group ended before this k-step
+            fold(cur_g);
+            ++cur_g;
+            next_fold = min(next_fold + p.gs, kend);
+            set_zeros(cur_g);
+          }
         }
-      }
-      uint32_t b[MT][2];
-#pragma unroll
-      for (int mt = 0; mt < MT; ++mt) {
-        const uint2 v = lds64(base + L.x_off() + (mt * 8 + g) * XP + ks * 32 + t * 8);
-        b[mt][0] = v.x;
-        b[mt][1] = v.y;
-      }
-      const int h = ks / WK, j = ks % WK;
-#pragma unroll
-      for (int ti = 0; ti < TN; ++ti) {
-        const uint32_t wg = h ? wv[ti].z : wv[ti].x;
-        const uint32_t wg8 = h ? wv[ti].w : wv[ti].y;
-        uint32_t a0, a1, a2, a3;
-        if constexpr (W == 8) {
-          a0 = int8_pair<BF16>(wg, 0);
-          a1 = int8_pair<BF16>(wg8, 0);
-          a2 = int8_pair<BF16>(wg, 1);
-          a3 = int8_pair<BF16>(wg8, 1);
-        } else if constexpr (kOddFma) {
-          // fields 2j and 2j + 1 from one shift by 8 j
-          const uint32_t v = wg >> (8 * j), v8 = wg8 >> (8 * j);
-          a0 = sub_pair<false>(and_or(v, 0x000F000Fu, Magic<false>::kPair), zz[ti][0]);
-          a1 = sub_pair<false>(and_or(v8, 0x000F000Fu, Magic<false>::kPair), zz[ti][1]);
-          a2 = fma_h2(and_or(v, 0x00F000F0u, Magic<false>::kPair), kF16Sixteenth, zz16[ti][0]);
-          a3 = fma_h2(and_or(v8, 0x00F000F0u, Magic<false>::kPair), kF16Sixteenth, zz16[ti][1]);
-        } else {
-          a0 = sub_pair<BF16>(code_pair<W, BF16>(wg, 2 * j), zz[ti][0]);
-          a1 = sub_pair<BF16>(code_pair<W, BF16>(wg8, 2 * j), zz[ti][1]);
-          a2 = sub_pair<BF16>(code_pair<W, BF16>(wg, 2 * j + 1), zz[ti][0]);
-          a3 = sub_pair<BF16>(code_pair<W, BF16>(wg8, 2 * j + 1), zz[ti][1]);
-        }
+        uint32_t b[MT][2];
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
-          if (GROUPED)
-            mma16816<BF16>(accg[ti][mt], a0, a1, a2, a3, b[mt][0], b[mt][1]);
-          else
-            mma16816<BF16>(acc[ti][mt], a0, a1, a2, a3, b[mt][0], b[mt][1]);
+          const uint2 v = lds64(base + L.x_off() + (mt * 8 + g) * XP + ks * 32 + t * 8);
+          b[mt][0] = v.x;
+          b[mt][1] = v.y;
+        }
+        const int h = ks / WK, j = ks % WK;
+#pragma unroll
+        for (int ti = 0; ti < TN; ++ti) {
+          const uint32_t wg = h ? wv[ti].z : wv[ti].x;
+          const uint32_t wg8 = h ? wv[ti].w : wv[ti].y;
+          uint32_t a0, a1, a2, a3;
+          if constexpr (W == 8) {
+            a0 = int8_pair<BF16>(wg, 0);
+            a1 = int8_pair<BF16>(wg8, 0);
+            a2 = int8_pair<BF16>(wg, 1);
+            a3 = int8_pair<BF16>(wg8, 1);
+          } else if constexpr (kOddFma) {
+            // fields 2j and 2j + 1 from one shift by 8 j
+            const uint32_t v = wg >> (8 * j), v8 = wg8 >> (8 * j);
+            a0 = sub_pair<false>(and_or(v, 0x000F000Fu, Magic<false>::kPair), zz[ti][0]);
+            a1 = sub_pair<false>(and_or(v8, 0x000F000Fu, Magic<false>::kPair), zz[ti][1]);
+            a2 = fma_h2(and_or(v, 0x00F000F0u, Magic<false>::kPair), kF16Sixteenth, zz16[ti][0]);
+            a3 = fma_h2(and_or(v8, 0x00F000F0u, Magic<false>::kPair), kF16Sixteenth, zz16[ti][1]);
+          } else {
+            a0 = sub_pair<BF16>(code_pair<W, BF16>(wg, 2 * j), zz[ti][0]);
+            a1 = sub_pair<BF16>(code_pair<W, BF16>(wg8, 2 * j), zz[ti][1]);
+            a2 = sub_pair<BF16>(code_pair<W, BF16>(wg, 2 * j + 1), zz[ti][0]);
+            a3 = sub_pair<BF16>(code_pair<W, BF16>(wg8, 2 * j + 1), zz[ti][1]);
+          }
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt) {
+            if (GROUPED)
+              mma16816<BF16>(accg[ti][mt], a0, a1, a2, a3, b[mt][0], b[mt][1]);
+            else
+              mma16816<BF16>(acc[ti][mt], a0, a1, a2, a3, b[mt][0], b[mt][1]);
+          }
         }
       }
-    }
+    }  // slots of the stage
     mbar_arrive(smem_addr(&empty[st]));  // this lane is done with the stage
     st = st1;
     ph = ph1;
