@@ -308,6 +308,20 @@ def cpu_measure(p, steps, warmup, min_seconds=0.0):
     return wbytes / dt / 1e9, threads, sample, dt
 
 
+def max_over_ranks(sec, dist, torch, device="cuda"):
+    """The job's time: the slowest rank's (every rank times the same number of steps)."""
+    if dist is None:
+        return sec
+    t = torch.tensor([sec], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gbps(world, weight_bytes, steps, sec):
+    """Whole-job throughput: the weight bytes every rank streamed over the job's time."""
+    return world * weight_bytes * steps / sec / 1e9
+
+
 def get_problem(args):
     from weight_only_quantized_wq_gb300 import synthetic as syn
     f = syn.WORKLOADS[args.workload]
@@ -373,12 +387,9 @@ def main():
     sec = time_graphs(p, sets, ws, args.steps, args.warmup, torch, wq, hold_s=0 if args.kernel_only else args.hold_s,
                       dist=dist)
     clk = None if args.kernel_only else clocks.stop()
-    if dist is not None:
-        t = torch.tensor([sec], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        sec = float(t.item())
+    sec = max_over_ranks(sec, dist, torch)
     per_step = sec / args.steps
-    value = world * p.weight_bytes() * args.steps / sec / 1e9
+    value = job_gbps(world, p.weight_bytes(), args.steps, sec)
     lpc = launches_per_call(p)
     roof = roofline_entry(p, per_step, pk, pk_src)
     key = "%s|M=%d" % (args.workload, p.M)
@@ -390,7 +401,8 @@ def main():
         e2e_sec, h2d, d2h = sec, 0, 0
     else:
         e2e_sec, h2d, d2h = time_e2e(p, sets, ws, args.steps, args.warmup, torch, wq)
-    e2e_val = world * p.weight_bytes() * args.steps / e2e_sec / 1e9
+    e2e_sec = max_over_ranks(e2e_sec, dist, torch)
+    e2e_val = job_gbps(world, p.weight_bytes(), args.steps, e2e_sec)
 
     line = {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(per_step * 1e3, 5), "higher_is_better": True,
