@@ -111,11 +111,6 @@ __device__ __forceinline__ void consumer_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(kDecodeWarps * 32) : "memory");
 }
 
-__device__ __forceinline__ uint4 ldg_nc128(const void *p) {
-  uint4 v;
-  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
-  return v;
-}
 
 template <int W, bool BF16, int MT, int TN, bool ZERO, int FOLD>
 __global__ void __launch_bounds__(kDecodeThreads, decode_min_blocks(MT, TN))

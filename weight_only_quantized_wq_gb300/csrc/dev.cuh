@@ -99,11 +99,6 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
   return pol;
 }
-__device__ __forceinline__ uint64_t policy_evict_last() {
-  uint64_t pol;
-  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
-  return pol;
-}
 
 // 1-D bulk copy global -> this CTA's shared memory, completing `bytes` of
 // transaction count on `bar`.  dst, src 16-byte aligned; bytes % 16 == 0.
@@ -128,16 +123,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, int 
       : "memory");
 }
 
-// 16-byte asynchronous copy global -> shared (cp.async, L2 only), and the
-// arrival on an mbarrier that fires once all of this thread's earlier
-// cp.async copies have landed (.noinc: the barrier's expected count already
-// includes this arrival).
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
-}
 
 // ---------------------------------------------------------------- clusters
 // Barrier over every thread of every CTA of the cluster (release / acquire).
