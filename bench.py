@@ -23,6 +23,7 @@ import glob
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -60,10 +61,19 @@ def peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+def _code_only(text: str) -> str:
+    """C/CUDA source with comments and blank space removed: edits to comments
+    or layout leave the compiled kernels, and so a capture of them, unchanged."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def sources_sha() -> str:
+    """Hash of the kernel sources' code, to tie an ncu capture to the kernels it measured."""
     h = hashlib.sha256()
     for f in sorted(glob.glob(os.path.join(ROOT, "weight_only_quantized_wq_gb300", "csrc", "*"))):
-        h.update(open(f, "rb").read())
+        h.update(os.path.basename(f).encode() + b"\0" + _code_only(open(f, encoding="utf-8").read()).encode())
     return h.hexdigest()[:16]
 
 

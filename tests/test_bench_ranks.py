@@ -52,3 +52,11 @@ def test_reference_arm_other_ranks_exit_without_work():
                        env=env, capture_output=True, text=True, timeout=120)
     assert r.returncode == 0, r.stderr
     assert r.stdout.strip() == ""
+
+
+def test_capture_hash_ignores_comments_not_code():
+    a = "int f(int x) { return x + 1; }  // one\n/* two */\n"
+    b = "// another comment\nint f(int x) {\n  return x + 1;\n}\n"
+    c = "int f(int x) { return x + 2; }\n"
+    assert bench._code_only(a) == bench._code_only(b)
+    assert bench._code_only(a) != bench._code_only(c)

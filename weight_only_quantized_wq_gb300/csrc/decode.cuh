@@ -5,13 +5,15 @@
 // from HBM once, through a deep shared-memory ring, and turned into
 // tensor-core operands in registers.
 //
-// Roles (5 warps): one producer lane issues, per ring stage (one chunk row of
-// KC values of K), a 1-D bulk copy of the packed weights of the CTA's 16*4*TN
-// output channels and a 2-D tensor copy of the activation slice; four
-// consumer warps (TN tiles of 16 channels each) wait for a stage, compute it
-// and release it.  Nothing else couples the warps: the scale and zero rows of
-// all of the CTA's groups are staged in shared memory once, at the start, so
-// a finished group is folded without waiting for anyone.
+// Roles (5 warps): one producer lane first copies the scale rows and the
+// packed zero-word rows of all of the CTA's groups (two 2-D tensor copies),
+// then, per slot of a ring stage (one chunk row of KC values of K; two slots
+// per stage), a 1-D bulk copy of the packed weights of the CTA's 16*4*TN
+// output channels and a 2-D tensor copy of the activation slice.  Four
+// consumer warps (TN tiles of 16 channels each) build the (MAGIC + zero)
+// pairs once, then wait for a stage, compute its slots and release it.
+// Nothing else couples the warps, so a finished group is folded without
+// waiting for anyone.
 //
 // Swap-AB: the weight tile (16 output channels x 16 k) is the A operand of
 // mma.m16n8k16 and the tokens are its N = 8 columns, so the output channels
