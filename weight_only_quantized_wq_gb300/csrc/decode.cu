@@ -211,7 +211,7 @@ cudaError_t launch_decode(const MatmulArgs &a, const DecodePlan &p, void *worksp
     dp.counters = static_cast<int *>(workspace);
     dp.partial = reinterpret_cast<float *>(static_cast<char *>(workspace) + decode_counter_bytes());
   }
-  // Tensor map of the activation slice of a stage (rows past M read as zeros).
+  // Tensor map of the activation slice of a slot (rows past M read as zeros).
   if (!encode_2d(&dp.tm_x, a.x, (uint64_t)a.K, (uint64_t)a.M, (uint32_t)(x_pitch(a.w_bit) / 2), (uint32_t)(p.mt * 8)))
     return cudaErrorInvalidValue;
   // Scale rows and zero-word rows of a CTA: one box of (CTA columns x rows) each.
