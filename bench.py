@@ -218,25 +218,50 @@ def launches_per_call(p) -> int:
 
 
 def time_e2e(p, sets, ws, steps, warmup, torch, wq):
-    """Public API with host buffers: per step H2D of x from pinned memory,
-    wq_matmul, D2H of y into pinned memory; CUDA events on the same stream."""
+    """Public API with host buffers, as a serving loop runs it: every step copies
+    its x from pinned host memory (H2D stream), calls wq_matmul (the launching
+    stream) and copies its y back to pinned host memory (D2H stream).  Events
+    order each step's copies around its call, and a buffer set is reused only
+    after its previous y has reached the host, so the copies of one step overlap
+    the kernels of its neighbours.  CUDA events on the launching stream bracket
+    all steps (it waits for the last D2H copy before the closing event)."""
+    n = len(sets)
     xh = [s["x"].cpu().pin_memory() for s in sets]
-    yh = torch.empty((p.M, p.N), dtype=torch.float32).pin_memory()
+    yh = [torch.empty((p.M, p.N), dtype=torch.float32).pin_memory() for _ in range(n)]
+    main = torch.cuda.current_stream()
+    h2d_s, d2h_s = torch.cuda.Stream(), torch.cuda.Stream()
+    x_in = [torch.cuda.Event() for _ in range(n)]
+    y_out = [torch.cuda.Event() for _ in range(n)]
+    y_home = [torch.cuda.Event() for _ in range(n)]  # the set's last y is in host memory
+    used = [False] * n
 
     def step(i):
-        s = sets[i % len(sets)]
-        s["x"].copy_(xh[i % len(sets)], non_blocking=True)
+        k = i % n
+        s = sets[k]
+        with torch.cuda.stream(h2d_s):
+            if used[k]:
+                h2d_s.wait_event(y_home[k])
+            s["x"].copy_(xh[k], non_blocking=True)
+            x_in[k].record(h2d_s)
+        main.wait_event(x_in[k])
         call(p, s, wq, ws)
-        yh.copy_(s["out"], non_blocking=True)
+        y_out[k].record(main)
+        with torch.cuda.stream(d2h_s):
+            d2h_s.wait_event(y_out[k])
+            yh[k].copy_(s["out"], non_blocking=True)
+            y_home[k].record(d2h_s)
+        used[k] = True
 
     for i in range(warmup):
         step(i)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
+    e0.record(main)
+    h2d_s.wait_event(e0)  # the first copy starts inside the timed region
     for i in range(steps):
         step(i)
-    e1.record()
+    main.wait_stream(d2h_s)
+    e1.record(main)
     torch.cuda.synchronize()
     h2d = p.x.numel() * p.x.element_size()
     return e0.elapsed_time(e1) / 1e3, h2d, p.M * p.N * 4

@@ -115,19 +115,23 @@ def wq_workspace_bytes(M: int, N: int, K: int, w_bit: int, group_size: int) -> i
 
 
 _workspaces: dict = {}
+_needs: dict = {}
 
 
 def workspace_for(M, N, K, w_bit, group_size, device) -> torch.Tensor | None:
     """A zero-filled workspace big enough for this problem, cached per device.
     Completed calls leave it reusable (its counters back at zero)."""
-    need = wq_workspace_bytes(M, N, K, w_bit, group_size)
+    dkey = torch.device(device).index
+    nkey = (dkey, M, N, K, w_bit, group_size)
+    need = _needs.get(nkey)
+    if need is None:
+        need = _needs[nkey] = wq_workspace_bytes(M, N, K, w_bit, group_size)
     if need == 0:
         return None
-    key = torch.device(device).index
-    ws = _workspaces.get(key)
+    ws = _workspaces.get(dkey)
     if ws is None or ws.numel() < need:
         ws = torch.zeros(need, dtype=torch.uint8, device=device)
-        _workspaces[key] = ws
+        _workspaces[dkey] = ws
     return ws
 
 

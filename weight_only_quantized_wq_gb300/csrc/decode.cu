@@ -112,7 +112,7 @@ static long capacity(int w_bit, int fold, int mt, int tn, bool zero, int smem, i
   return c;
 }
 
-DecodePlan plan_decode(int M, int N, int K, int w_bit, int group_size, bool zero, int sms) {
+static DecodePlan plan_decode_search(int M, int N, int K, int w_bit, int group_size, bool zero, int sms) {
   DecodePlan best{};
   const int rows = M < 64 ? M : 64;
   const int mt = rows <= 8 ? 1 : rows <= 16 ? 2 : rows <= 32 ? 4 : 8;
@@ -185,6 +185,27 @@ DecodePlan plan_decode(int M, int N, int K, int w_bit, int group_size, bool zero
                        ? decode_counter_bytes() + (size_t)best.splits * rows * N * sizeof(float)
                        : 0;
   return best;
+}
+
+// The plan of a shape, searched once per device and shape (a call then costs
+// one lookup instead of a search over every split count).
+DecodePlan plan_decode(int M, int N, int K, int w_bit, int group_size, bool zero, int sms) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) dev = -1;
+  using Key = std::tuple<int, int, int, int, int, int, bool, int>;
+  static std::map<Key, DecodePlan> cache;
+  static std::mutex mu;
+  const Key key{dev, M, N, K, w_bit, group_size, zero, sms};
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+  }
+  const DecodePlan p = plan_decode_search(M, N, K, w_bit, group_size, zero, sms);
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache.size() > 4096) cache.clear();  // bounded: a process with many shapes searches again
+  cache.emplace(key, p);
+  return p;
 }
 
 cudaError_t launch_decode(const MatmulArgs &a, const DecodePlan &p, void *workspace, cudaStream_t s) {
