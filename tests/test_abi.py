@@ -98,3 +98,20 @@ def test_pack_host_validation(L):
 def test_workspace_bytes_invalid_is_zero(L):
     assert binding.wq_workspace_bytes(0, 64, 128, 4, 64) == 0
     assert binding.wq_workspace_bytes(4, 64, 100, 4, 64) == 0
+
+
+def test_binding_marshals_to_the_c_abi_and_raises_its_status():
+    # CPU tensors and a stand-in stream: the call crosses ctypes and the C side
+    # rejects it with a status, which the binding raises as WQError.
+    import torch
+    from weight_only_quantized_wq_gb300 import binding
+
+    class Stream:
+        cuda_stream = 0
+
+    x = torch.zeros(1, 512, dtype=torch.bfloat16)
+    q = torch.zeros(512 * 512 // 2, dtype=torch.uint8)
+    s = torch.zeros(4, 512, dtype=torch.bfloat16)
+    out = torch.zeros(1, 512)
+    with pytest.raises(binding.WQError):
+        binding.wq_matmul(x, q, s, None, 1, 512, 512, 4, 128, out=out, stream=Stream())

@@ -65,12 +65,12 @@ def lib() -> ctypes.CDLL:
 
 
 def _ptr(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    # plain ints: the c_void_p argtypes convert them (None is NULL)
+    return None if t is None else t.data_ptr()
 
 
 def _stream(stream=None):
-    s = stream if stream is not None else torch.cuda.current_stream()
-    return ctypes.c_void_p(s.cuda_stream)
+    return (stream if stream is not None else torch.cuda.current_stream()).cuda_stream
 
 
 def _check(st: int, what: str):

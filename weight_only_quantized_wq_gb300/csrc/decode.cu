@@ -29,10 +29,8 @@ static EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// Row-major 2-D tensor of 16- or 32-bit elements (rows x cols) and a box of
-// (box_cols x box_rows), no swizzle, zero fill outside the tensor.
-static bool encode_2d(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows, uint32_t box_cols,
-                      uint32_t box_rows, int elem_bytes = 2) {
+static bool encode_2d_new(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows, uint32_t box_cols,
+                          uint32_t box_rows, int elem_bytes) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[2] = {cols, rows};
@@ -43,6 +41,32 @@ static bool encode_2d(CUtensorMap *m, const void *base, uint64_t cols, uint64_t 
   return fn(m, dt, 2, const_cast<void *>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Row-major 2-D tensor of 16- or 32-bit elements (rows x cols) and a box of
+// (box_cols x box_rows), no swizzle, zero fill outside the tensor.  A map
+// holds only the address, sizes and box, so one encoded for the same six
+// values is reused (a serving loop passes the same weight, scale and
+// activation buffers every call).
+static bool encode_2d(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows, uint32_t box_cols,
+                      uint32_t box_rows, int elem_bytes = 2) {
+  using Key = std::tuple<uintptr_t, uint64_t, uint64_t, uint32_t, uint32_t, int>;
+  static std::map<Key, CUtensorMap> cache;
+  static std::mutex mu;
+  const Key key{reinterpret_cast<uintptr_t>(base), cols, rows, box_cols, box_rows, elem_bytes};
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) {
+      *m = it->second;
+      return true;
+    }
+  }
+  if (!encode_2d_new(m, base, cols, rows, box_cols, box_rows, elem_bytes)) return false;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache.size() > 1024) cache.clear();  // bounded
+  cache.emplace(key, *m);
+  return true;
 }
 
 // The workspace starts with a fixed region of kMaxColumnBlocks arrival
