@@ -32,8 +32,10 @@
  *     gives up (bounded spin on a shared-memory barrier) records a flag that
  *     wq_check_device() turns into WQ_ERR_TIMEOUT; the kernel then returns
  *     without faulting.
- *   - The library keeps no state besides a per-device cache of the SM count
- *     and the kernels' shared-memory attributes.
+ *   - The library keeps no state besides per-device caches (SM count,
+ *     kernel attributes, launch plans, tensor maps, the device addresses of
+ *     its own __device__ variables).  cudaDeviceReset while the library is
+ *     in use is not supported: those cached addresses would be stale.
  */
 #ifndef WQ_H
 #define WQ_H
@@ -67,18 +69,33 @@ typedef enum {
 
 typedef enum { WQ_F16 = 0, WQ_BF16 = 1, WQ_F32 = 2 } wq_dtype;
 
-/* Human-readable name of a status; never NULL. */
+/*
+ * Human-readable name of a status; never NULL.
+ * The statuses stand for the argument checks the pages make before a launch:
+ * the TORCH_CHECKs of marlin_gemm and marlin_cuda (aphrodite-engine
+ * marlin_cuda_kernel.cu: shape mismatches, K and N not divisible by the tile,
+ * group size, workspace below its minimum) and the ValueError of tiny-llm
+ * int8_matmul (kernels/int8_gemv.py: M above MAX_M, K mismatch, x not
+ * bf16/fp16).  Here they are returned as codes, since no exception may cross
+ * a C ABI.
+ */
 WQ_API const char *wq_status_string(wq_status s);
 
 /*
  * Number of values along K that one packed chunk row spans: 256 / w_bit
- * (128 for w_bit 2, 64 for 4, 32 for 8).  K must be a multiple of it.
+ * (128 for w_bit 2, 64 for 4, 32 for 8).  K must be a multiple of it.  It
+ * plays the part of Marlin's tile_size check on size_k (marlin_gemm,
+ * aphrodite-engine marlin_cuda_kernel.cu): the tiled layout is only defined
+ * for whole chunk rows.
  */
 WQ_API int wq_chunk_k(int w_bit);
 
 /*
  * Bytes of the packed weight buffer that wq_pack writes: K * N * w_bit / 8,
- * the same count as the input.  Returns 0 for an invalid shape or w_bit.
+ * the same count as the input, whose shape the BitDistiller
+ * quant_matmul_kernel docstring gives as qw: (K // pack_num, N) int32 with
+ * pack_num = 32 / w_bit (and tiny-llm int8_matmul as q: (N, K) int8).
+ * Returns 0 for an invalid shape or w_bit.
  */
 WQ_API size_t wq_packed_bytes(int K, int N, int w_bit);
 
@@ -103,11 +120,20 @@ WQ_API wq_status wq_pack(const void *q_in, int K, int N, int w_bit, void *packed
  * wq_unpack -- inverse of wq_pack for tests and tooling.
  * codes_out: uint8 (K, N) row-major; code of (k, n) for w_bit 2/4, and the
  *   two's-complement byte of q[n, k] for w_bit 8.
+ * The code of (k, n) is the field the K loop of BitDistiller
+ * quant_matmul_kernel extracts from qw (K // pack_num, N):
+ * (qw[k / pack_num][n] >> ((k % pack_num) * w_bit)) & (2^w_bit - 1).
+ * Same requirements and statuses as wq_pack (packed 16-byte aligned).
  */
 WQ_API wq_status wq_unpack(const void *packed, int K, int N, int w_bit, uint8_t *codes_out, void *stream);
 
 /*
  * Bytes of scratch memory wq_matmul needs for this problem (0 if none).
+ * It stands for the workspace of marlin_gemm (aphrodite-engine
+ * marlin_cuda_kernel.cu), whose size check requires at least
+ * (size_n / min_thread_n) * max_par ints of zero-filled lock counters for its
+ * reduction across thread blocks along K; here the counters are followed by
+ * fp32 partial sums (see below) and most shapes need none at all.
  * The workspace holds a fixed 16 KiB block of int32 arrival counters (one per
  * column block) followed by the fp32 partial sums of a split along K.  It
  * must be zero-filled before its first use; every completed call leaves the
@@ -116,7 +142,9 @@ WQ_API wq_status wq_unpack(const void *packed, int K, int N, int w_bit, uint8_t 
  * run concurrently (they would race on the counters and partials).
  * The split along K (and so this size) is chosen with the runtime's occupancy
  * calculator for the current device; the answer covers both the asymmetric
- * (zeros given) and the symmetric case.
+ * (zeros given) and the symmetric case and every x / scale dtype, so it may
+ * exceed what a given call needs (a call on the tensor-core path for many
+ * tokens needs none).
  */
 WQ_API size_t wq_workspace_bytes(int M, int N, int K, int w_bit, int group_size);
 
@@ -182,6 +210,10 @@ WQ_API wq_status wq_matmul_noalloc(const void *x, wq_dtype x_dtype, const void *
  * wq_check_device -- synchronise `stream`, then read and clear the device
  * word in which kernels record a barrier wait that gave up.  Returns
  * WQ_ERR_TIMEOUT if one did, WQ_ERR_CUDA on a runtime error, else WQ_OK.
+ * The pages have no status path of this kind: the barrier_acquire of
+ * Marlin's cross-block reduction (aphrodite-engine marlin_cuda_kernel.cu)
+ * spins on its lock without a limit.  Every wait of this library is bounded
+ * and reports here instead of hanging the device.
  */
 WQ_API wq_status wq_check_device(void *stream);
 

@@ -188,5 +188,44 @@ def pin_slicing(orc):
     assert np.array_equal(p8, f8[[1, 3], 2:11])
 
 
+def _pack_np(codes, wb):
+    """Page-layout packing written out with numpy shifts (independent of the
+    oracle's packer): field k % pack of word [k // pack][n], LSB first."""
+    K, N = codes.shape
+    pk = 32 // wb
+    words = np.zeros(((K + pk - 1) // pk, N), dtype=np.uint64)
+    for k in range(K):
+        words[k // pk] |= codes[k].astype(np.uint64) << np.uint64(wb * (k % pk))
+    return words.astype(np.uint32).view(np.int32)
+
+
+def pin_dequant_closed_form(orc):
+    """dequant(qw, s, qz)[k, n] == (code - zero[g, n]) * scale[g, n], g = k // group_size,
+    computed with numpy from the codes, zeros and scales the test drew (scales
+    widened by torch's own cast); symmetric (no qzeros) uses zero 2^(w_bit - 1).
+    One-hot rows of x through matmul_grouped give the same rows exactly."""
+    rng = np.random.default_rng(8)
+    for wb, (K, N, gs), sbf in ((4, (96, 5, 32), True), (2, (128, 3, 64), False), (4, (64, 4, 64), False)):
+        G = K // gs
+        codes = rng.integers(0, 2 ** wb, (K, N), dtype=np.uint8)
+        zeros = rng.integers(0, 2 ** wb, (G, N), dtype=np.uint8)
+        sc = torch.tensor(rng.uniform(0.003, 3.0, (G, N)), dtype=torch.bfloat16 if sbf else torch.float16)
+        s64 = sc.to(torch.float64).numpy()
+        sbits = sc.view(torch.int16).numpy().view(np.uint16)
+        qw = _pack_np(codes, wb)
+        for qz, z in ((_pack_np(zeros, wb), zeros.astype(np.float64)),
+                      (None, np.full((G, N), 2.0 ** (wb - 1)))):
+            got = orc.dequant(qw, sbits, sbf, qz, K, N, wb, gs)
+            gi = np.arange(K) // gs
+            ref = (codes.astype(np.float64) - z[gi]) * s64[gi]
+            assert np.array_equal(got, ref), (wb, K, N, gs, qz is None)
+            for k in (0, gs - 1, K - 1):
+                x = np.zeros((1, K), dtype=np.float16)
+                x[0, k] = 1.0
+                y = orc.matmul_grouped(x.view(np.uint16), False, qw, sbits, sbf, qz, 1, N, K, wb, gs)
+                assert np.array_equal(y[0], got[k]), (wb, k)
+
+
 ALL_PINS = [pin_golden, pin_decoders, pin_pack_identity, pin_numpy_integer_matmul,
-            pin_grouped_closed_form, pin_symmetric_equals_zero8, pin_int8_numpy, pin_slicing]
+            pin_grouped_closed_form, pin_symmetric_equals_zero8, pin_int8_numpy, pin_slicing,
+            pin_dequant_closed_form]

@@ -102,16 +102,26 @@ def test_workspace_bytes_invalid_is_zero(L):
 
 def test_binding_marshals_to_the_c_abi_and_raises_its_status():
     # CPU tensors and a stand-in stream: the call crosses ctypes and the C side
-    # rejects it with a status, which the binding raises as WQError.
+    # rejects it with a status, which the binding raises as WQError.  x is a
+    # view two bytes into its buffer, so the alignment check of wq_matmul
+    # (which runs before any device query or launch) returns WQ_ERR_ALIGN on
+    # every machine, with or without a GPU: nothing is ever launched on these
+    # host pointers.
     import torch
     from weight_only_quantized_wq_gb300 import binding
 
     class Stream:
         cuda_stream = 0
 
-    x = torch.zeros(1, 512, dtype=torch.bfloat16)
+    xbuf = torch.zeros(1, 512 + 8, dtype=torch.bfloat16)
+    x = xbuf[:, 1:513]
+    assert x.data_ptr() % 16 == 2
     q = torch.zeros(512 * 512 // 2, dtype=torch.uint8)
     s = torch.zeros(4, 512, dtype=torch.bfloat16)
     out = torch.zeros(1, 512)
-    with pytest.raises(binding.WQError):
+    with pytest.raises(binding.WQError) as e:
         binding.wq_matmul(x, q, s, None, 1, 512, 512, 4, 128, out=out, stream=Stream())
+    assert e.value.status == binding.STATUS.index("WQ_ERR_ALIGN")
+    with pytest.raises(binding.WQError) as e:
+        binding.wq_matmul_noalloc(x, q, s, None, 1, 512, 512, 4, 128, out=out, stream=Stream())
+    assert e.value.status == binding.STATUS.index("WQ_ERR_ALIGN")

@@ -34,6 +34,9 @@ MUTANTS = {
     "symmetric-zero": ("return (double)(1 << (w_bit - 1));", "return (double)(1 << w_bit);"),
     "int8-scale-index": ("wq_oracle_f32_to_f64(scale_bits[n]) * acc", "wq_oracle_f32_to_f64(scale_bits[0]) * acc"),
     "group-index": ("int g = k / group_size;\n        /* row k", "int g = (k / group_size) / 2;\n        /* row k"),
+    "dequant-zero-sign": ("w[(size_t)k * N + n] = (q - z) * s;", "w[(size_t)k * N + n] = (q + z) * s;"),
+    "dequant-scale-row": ("double s = decode16(scales[(size_t)g * N + n], s_is_bf16);\n            w[",
+                          "double s = decode16(scales[(size_t)(k % (K / group_size)) * N + n], s_is_bf16);\n            w["),
 }
 
 CHILD = r"""

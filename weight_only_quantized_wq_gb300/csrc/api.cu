@@ -7,6 +7,7 @@
 
 #include <cuda_runtime.h>
 
+#include "api.h"
 #include "kernels.h"
 #include "wq.h"
 
@@ -80,6 +81,73 @@ size_t slice_workspace(int M, int N, int K, int w_bit, int group_size, bool zero
 
 }  // namespace
 
+namespace wq {
+
+wq_status prepare_call(const void *x, wq_dtype x_dtype, const void *packed_w, const void *scales, wq_dtype s_dtype,
+                       const int32_t *zeros, int M, int N, int K, int w_bit, int group_size, float *out, Call *c) {
+  *c = Call{};
+  if (!x || !packed_w || !scales || !out) return WQ_ERR_NULL;
+  if (!valid_wbit(w_bit)) return WQ_ERR_WBIT;
+  if (M < 0 || N < 0 || K <= 0) return WQ_ERR_SHAPE;
+  if (M == 0 || N == 0) {
+    c->noop = true;
+    return WQ_OK;
+  }
+  wq_status st = check_kn(K, N, w_bit);
+  if (st != WQ_OK) return st;
+  if (x_dtype != WQ_F16 && x_dtype != WQ_BF16) return WQ_ERR_DTYPE;
+  if (w_bit == 8) {
+    if (s_dtype != WQ_F32 || zeros != nullptr) return WQ_ERR_DTYPE;
+    group_size = K;
+  } else {
+    if (s_dtype != WQ_F16 && s_dtype != WQ_BF16) return WQ_ERR_DTYPE;
+    if (group_size == -1) group_size = K;
+    if (group_size <= 0 || K % group_size != 0 || group_size % 16 != 0) return WQ_ERR_GROUP;
+  }
+  if (!aligned(x, 16) || !aligned(packed_w, 16) || !aligned(out, 16) || !aligned(scales, 16) || !aligned(zeros, 16))
+    return WQ_ERR_ALIGN;
+  DeviceInfo *d = nullptr;
+  if ((st = device_info(&d)) != WQ_OK) return st;
+  MatmulArgs &a = c->a;
+  a.x = x;
+  a.packed = packed_w;
+  a.scales = scales;
+  a.zeros = reinterpret_cast<const uint32_t *>(zeros);
+  a.out = out;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.w_bit = w_bit;
+  a.group_size = group_size;
+  a.x_bf16 = (x_dtype == WQ_BF16);
+  a.s_bf16 = (s_dtype == WQ_BF16);
+  a.err = d->status;
+  c->sms = d->sms;
+  c->prefill = M >= kPrefillMinM && prefill_supported(a);
+  c->need = c->prefill ? 0 : slice_workspace(M, N, K, w_bit, group_size, zeros != nullptr, d->sms);
+  return WQ_OK;
+}
+
+wq_status run_call(const Call &c, void *workspace, void *stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (c.prefill) return launch_prefill(c.a, s) == cudaSuccess ? WQ_OK : WQ_ERR_CUDA;
+  // Rows are processed 64 at a time (the few-token kernel's largest token tile).
+  MatmulArgs a = c.a;
+  const int M = c.a.M, N = a.N, K = a.K;
+  const bool zero = a.zeros != nullptr;
+  const DecodePlan full = plan_decode(M < 64 ? M : 64, N, K, a.w_bit, a.group_size, zero, c.sms);
+  for (int m0 = 0; m0 < M; m0 += 64) {
+    a.M = (M - m0) < 64 ? (M - m0) : 64;
+    a.x = static_cast<const uint16_t *>(c.a.x) + (size_t)m0 * K;
+    a.out = c.a.out + (size_t)m0 * N;
+    const DecodePlan p = (a.M == (M < 64 ? M : 64)) ? full : plan_decode(a.M, N, K, a.w_bit, a.group_size, zero, c.sms);
+    if (launch_decode(a, p, workspace, s) != cudaSuccess) return WQ_ERR_CUDA;
+  }
+  return WQ_OK;
+}
+
+}  // namespace wq
+
 extern "C" {
 
 const char *wq_status_string(wq_status s) {
@@ -145,61 +213,14 @@ size_t wq_workspace_bytes(int M, int N, int K, int w_bit, int group_size) {
 wq_status wq_matmul(const void *x, wq_dtype x_dtype, const void *packed_w, const void *scales, wq_dtype s_dtype,
                     const int32_t *zeros, int M, int N, int K, int w_bit, int group_size, float *out,
                     void *workspace, size_t workspace_bytes, void *stream) {
-  if (!x || !packed_w || !scales || !out) return WQ_ERR_NULL;
-  if (!valid_wbit(w_bit)) return WQ_ERR_WBIT;
-  if (M < 0 || N < 0 || K <= 0) return WQ_ERR_SHAPE;
-  if (M == 0 || N == 0) return WQ_OK;
-  wq_status st = check_kn(K, N, w_bit);
-  if (st != WQ_OK) return st;
-  if (x_dtype != WQ_F16 && x_dtype != WQ_BF16) return WQ_ERR_DTYPE;
-  if (w_bit == 8) {
-    if (s_dtype != WQ_F32 || zeros != nullptr) return WQ_ERR_DTYPE;
-    group_size = K;
-  } else {
-    if (s_dtype != WQ_F16 && s_dtype != WQ_BF16) return WQ_ERR_DTYPE;
-    if (group_size == -1) group_size = K;
-    if (group_size <= 0 || K % group_size != 0 || group_size % 16 != 0) return WQ_ERR_GROUP;
-  }
-  if (!aligned(x, 16) || !aligned(packed_w, 16) || !aligned(out, 16) || !aligned(scales, 16) || !aligned(zeros, 16))
-    return WQ_ERR_ALIGN;
-  DeviceInfo *d = nullptr;
-  if ((st = device_info(&d)) != WQ_OK) return st;
-
-  const bool zero = zeros != nullptr;
-  const size_t need = slice_workspace(M, N, K, w_bit, group_size, zero, d->sms);
-  if (need > 0) {
-    if (!workspace || workspace_bytes < need) return WQ_ERR_WORKSPACE;
+  wq::Call c;
+  wq_status st = wq::prepare_call(x, x_dtype, packed_w, scales, s_dtype, zeros, M, N, K, w_bit, group_size, out, &c);
+  if (st != WQ_OK || c.noop) return st;
+  if (c.need > 0) {
+    if (!workspace || workspace_bytes < c.need) return WQ_ERR_WORKSPACE;
     if (!aligned(workspace, 16)) return WQ_ERR_ALIGN;
   }
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  wq::MatmulArgs a{};
-  a.packed = packed_w;
-  a.scales = scales;
-  a.zeros = reinterpret_cast<const uint32_t *>(zeros);
-  a.N = N;
-  a.K = K;
-  a.w_bit = w_bit;
-  a.group_size = group_size;
-  a.x_bf16 = (x_dtype == WQ_BF16);
-  a.s_bf16 = (s_dtype == WQ_BF16);
-  a.err = d->status;
-  if (M >= wq::kPrefillMinM) {
-    a.M = M;
-    a.x = x;
-    a.out = out;
-    if (wq::prefill_supported(a)) return wq::launch_prefill(a, s) == cudaSuccess ? WQ_OK : WQ_ERR_CUDA;
-  }
-  // Otherwise rows are processed 64 at a time (the few-token kernel's largest token tile).
-  const wq::DecodePlan full = wq::plan_decode(M < 64 ? M : 64, N, K, w_bit, group_size, zero, d->sms);
-  for (int m0 = 0; m0 < M; m0 += 64) {
-    a.M = (M - m0) < 64 ? (M - m0) : 64;
-    a.x = static_cast<const uint16_t *>(x) + (size_t)m0 * K;
-    a.out = out + (size_t)m0 * N;
-    const wq::DecodePlan p =
-        (a.M == (M < 64 ? M : 64)) ? full : wq::plan_decode(a.M, N, K, w_bit, group_size, zero, d->sms);
-    if (wq::launch_decode(a, p, workspace, s) != cudaSuccess) return WQ_ERR_CUDA;
-  }
-  return WQ_OK;
+  return wq::run_call(c, workspace, stream);
 }
 
 wq_status wq_check_device(void *stream) {

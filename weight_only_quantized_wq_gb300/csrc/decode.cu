@@ -10,65 +10,6 @@
 
 namespace wq {
 
-// cuTensorMapEncodeTiled through the runtime's driver entry point (no libcuda link).
-typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
-                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-static EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    void *f = nullptr;
-    cudaDriverEntryPointQueryResult q{};
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(f);
-    tried = true;
-  }
-  return fn;
-}
-
-static bool encode_2d_new(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows, uint32_t box_cols,
-                          uint32_t box_rows, int elem_bytes) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
-  const cuuint64_t dims[2] = {cols, rows};
-  const cuuint64_t strides[1] = {cols * (uint64_t)elem_bytes};
-  const cuuint32_t box[2] = {box_cols, box_rows};
-  const cuuint32_t estr[2] = {1, 1};
-  const CUtensorMapDataType dt = elem_bytes == 4 ? CU_TENSOR_MAP_DATA_TYPE_UINT32 : CU_TENSOR_MAP_DATA_TYPE_UINT16;
-  return fn(m, dt, 2, const_cast<void *>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// Row-major 2-D tensor of 16- or 32-bit elements (rows x cols) and a box of
-// (box_cols x box_rows), no swizzle, zero fill outside the tensor.  A map
-// holds only the address, sizes and box, so one encoded for the same six
-// values is reused (a serving loop passes the same weight, scale and
-// activation buffers every call).
-static bool encode_2d(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows, uint32_t box_cols,
-                      uint32_t box_rows, int elem_bytes = 2) {
-  using Key = std::tuple<uintptr_t, uint64_t, uint64_t, uint32_t, uint32_t, int>;
-  static std::map<Key, CUtensorMap> cache;
-  static std::mutex mu;
-  const Key key{reinterpret_cast<uintptr_t>(base), cols, rows, box_cols, box_rows, elem_bytes};
-  {
-    std::lock_guard<std::mutex> lock(mu);
-    auto it = cache.find(key);
-    if (it != cache.end()) {
-      *m = it->second;
-      return true;
-    }
-  }
-  if (!encode_2d_new(m, base, cols, rows, box_cols, box_rows, elem_bytes)) return false;
-  std::lock_guard<std::mutex> lock(mu);
-  if (cache.size() > 1024) cache.clear();  // bounded
-  cache.emplace(key, *m);
-  return true;
-}
-
 // The workspace starts with a fixed region of kMaxColumnBlocks arrival
 // counters (enough for N up to 16 * 4 * kMaxColumnBlocks), so that counters
 // never share bytes with the fp32 partials that follow, whatever M and N a
@@ -257,15 +198,15 @@ cudaError_t launch_decode(const MatmulArgs &a, const DecodePlan &p, void *worksp
     dp.partial = reinterpret_cast<float *>(static_cast<char *>(workspace) + decode_counter_bytes());
   }
   // Tensor map of the activation slice of a slot (rows past M read as zeros).
-  if (!encode_2d(&dp.tm_x, a.x, (uint64_t)a.K, (uint64_t)a.M, (uint32_t)(x_pitch(a.w_bit) / 2), (uint32_t)(p.mt * 8)))
+  if (!encode_2d(&dp.tm_x, a.x, 2, (uint64_t)a.K, (uint64_t)a.M, (uint32_t)(x_pitch(a.w_bit) / 2), (uint32_t)(p.mt * 8)))
     return cudaErrorInvalidValue;
   // Scale rows and zero-word rows of a CTA: one box of (CTA columns x rows) each.
   const uint32_t cols = (uint32_t)(kDecodeWarps * p.tn * 16);
   if (a.w_bit != 8) {
     const int G = a.K / a.group_size, V = 32 / a.w_bit;
-    if (!encode_2d(&dp.tm_s, a.scales, (uint64_t)a.N, (uint64_t)G, cols, (uint32_t)p.srows))
+    if (!encode_2d(&dp.tm_s, a.scales, 2, (uint64_t)a.N, (uint64_t)G, cols, (uint32_t)p.srows))
       return cudaErrorInvalidValue;
-    if (a.zeros && !encode_2d(&dp.tm_z, a.zeros, (uint64_t)a.N, (uint64_t)((G + V - 1) / V), cols, (uint32_t)p.zwrows, 4))
+    if (a.zeros && !encode_2d(&dp.tm_z, a.zeros, 4, (uint64_t)a.N, (uint64_t)((G + V - 1) / V), cols, (uint32_t)p.zwrows))
       return cudaErrorInvalidValue;
   }
   const bool z = a.zeros != nullptr;

@@ -3,9 +3,17 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace wq {
+
+// Row-major 2-D tensor map of rows x cols elements of elem_bytes (1, 2 or 4)
+// with a box of box_cols x box_rows, swizzle 0 (none), 32, 64 or 128 bytes,
+// zero fill outside the tensor.  A map holds only these values, so one
+// encoded for the same values is reused (cached, thread-safe).
+bool encode_2d(CUtensorMap *m, const void *base, int elem_bytes, uint64_t cols, uint64_t rows, uint32_t box_cols,
+               uint32_t box_rows, int swizzle = 0);
 
 cudaError_t launch_pack(const void *qin, void *out, int K, int N, int w_bit, cudaStream_t s);
 cudaError_t launch_unpack(const void *packed, uint8_t *codes, int K, int N, int w_bit, cudaStream_t s);

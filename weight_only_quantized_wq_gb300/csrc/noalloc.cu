@@ -17,6 +17,7 @@
 
 #include <cuda_runtime.h>
 
+#include "api.h"
 #include "kernels.h"
 #include "wq.h"
 
@@ -52,19 +53,20 @@ extern "C" {
 wq_status wq_matmul_noalloc(const void *x, wq_dtype x_dtype, const void *packed_w, const void *scales,
                             wq_dtype s_dtype, const int32_t *zeros, int M, int N, int K, int w_bit, int group_size,
                             float *out, void *stream) {
-  const size_t need = (M > 0 && N > 0) ? wq_workspace_bytes(M, N, K, w_bit, group_size) : 0;
-  if (need > kNoAllocScratchBytes) return WQ_ERR_WORKSPACE;
+  // Every argument check runs first: an invalid call enqueues nothing.
+  wq::Call c;
+  wq_status st = wq::prepare_call(x, x_dtype, packed_w, scales, s_dtype, zeros, M, N, K, w_bit, group_size, out, &c);
+  if (st != WQ_OK || c.noop) return st;
+  if (c.need > kNoAllocScratchBytes) return WQ_ERR_WORKSPACE;
   void *scratch = nullptr;
-  if (need > 0) {
-    wq_status st = scratch_for_current_device(&scratch);
-    if (st != WQ_OK) return st;
+  if (c.need > 0) {
+    if ((st = scratch_for_current_device(&scratch)) != WQ_OK) return st;
     // The arrival counters at the front of the scratch must start at zero;
     // the array keeps whatever the previous call left, so clear them here.
     if (cudaMemsetAsync(scratch, 0, wq::decode_counter_bytes(), static_cast<cudaStream_t>(stream)) != cudaSuccess)
       return WQ_ERR_CUDA;
   }
-  return wq_matmul(x, x_dtype, packed_w, scales, s_dtype, zeros, M, N, K, w_bit, group_size, out, scratch,
-                   need > 0 ? kNoAllocScratchBytes : 0, stream);
+  return wq::run_call(c, scratch, stream);
 }
 
 }  // extern "C"

@@ -325,37 +325,6 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
 }  // namespace pf
 
 // ------------------------------------------------------------------ host side
-typedef CUresult (*EncodeTiledFn2)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
-                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
-                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-static EncodeTiledFn2 encode_fn2() {
-  static EncodeTiledFn2 fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    void *f = nullptr;
-    cudaDriverEntryPointQueryResult q{};
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn2>(f);
-    tried = true;
-  }
-  return fn;
-}
-
-static bool enc(CUtensorMap *m, const void *base, int esize, uint64_t cols, uint64_t rows, uint32_t bc, uint32_t br,
-                CUtensorMapSwizzle sw) {
-  EncodeTiledFn2 fn = encode_fn2();
-  if (!fn) return false;
-  const cuuint64_t dims[2] = {cols, rows};
-  const cuuint64_t strides[1] = {cols * (uint64_t)esize};
-  const cuuint32_t box[2] = {bc, br};
-  const cuuint32_t estr[2] = {1, 1};
-  return fn(m, esize == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void *>(base),
-            dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 bool prefill_supported(const MatmulArgs &a) {
   return a.w_bit == 4 && a.group_size % pf::BK == 0 && a.K % pf::BK == 0 && a.x_bf16 == a.s_bf16;
 }
@@ -388,12 +357,12 @@ cudaError_t launch_prefill(const MatmulArgs &a, cudaStream_t s) {
   // One 128-token accumulator per CTA up to 128 tokens, two (256 tokens) beyond.
   const int ms = a.M <= pf::UM ? 1 : 2;
   const int bm = pf::UM * ms;
-  if (!enc(&pp.tm_x, a.x, 2, (uint64_t)a.K, (uint64_t)a.M, pf::BK, (uint32_t)bm, CU_TENSOR_MAP_SWIZZLE_128B))
+  if (!encode_2d(&pp.tm_x, a.x, 2, (uint64_t)a.K, (uint64_t)a.M, pf::BK, (uint32_t)bm, 128))
     return cudaErrorInvalidValue;
-  if (!enc(&pp.tm_s, a.scales, 2, (uint64_t)a.N, (uint64_t)G, pf::BN, 1, CU_TENSOR_MAP_SWIZZLE_NONE))
+  if (!encode_2d(&pp.tm_s, a.scales, 2, (uint64_t)a.N, (uint64_t)G, pf::BN, 1, 0))
     return cudaErrorInvalidValue;
   if (a.zeros &&
-      !enc(&pp.tm_z, a.zeros, 4, (uint64_t)a.N, (uint64_t)((G + 7) / 8), pf::BN, 1, CU_TENSOR_MAP_SWIZZLE_NONE))
+      !encode_2d(&pp.tm_z, a.zeros, 4, (uint64_t)a.N, (uint64_t)((G + 7) / 8), pf::BN, 1, 0))
     return cudaErrorInvalidValue;
   pp.packed = static_cast<const uint8_t *>(a.packed);
   pp.out = a.out;
