@@ -207,6 +207,20 @@ WQ_API wq_status wq_matmul_noalloc(const void *x, wq_dtype x_dtype, const void *
                                    float *out, void *stream);
 
 /*
+ * wq_matmul_path -- which kernel family wq_matmul runs for this problem:
+ * 0 the few-token kernel (TMA ring, register dequant, mma.sync, split-K in
+ * clusters), 1 the exact tensor-core kernel (tcgen05, q - zero exact, group
+ * scale in fp32), 2 the many-token tensor-core kernel (weight rounded once to
+ * the x dtype); -1 if wq_matmul would reject the arguments' sizes, w_bit or
+ * dtypes.  The split by token count plays the part of tiny-llm's MAX_M
+ * (kernels/int8_gemv.py: up to 64 rows per call on the few-token kernel,
+ * more left to a GEMM) and of Marlin's small- and large-batch thread
+ * configurations (aphrodite-engine marlin_cuda_kernel.cu).  No device is
+ * touched.
+ */
+WQ_API int wq_matmul_path(int M, int K, int w_bit, int group_size, wq_dtype x_dtype, wq_dtype s_dtype);
+
+/*
  * wq_check_device -- synchronise `stream`, then read and clear the device
  * word in which kernels record a barrier wait that gave up.  Returns
  * WQ_ERR_TIMEOUT if one did, WQ_ERR_CUDA on a runtime error, else WQ_OK.

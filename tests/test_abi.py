@@ -125,3 +125,26 @@ def test_binding_marshals_to_the_c_abi_and_raises_its_status():
     with pytest.raises(binding.WQError) as e:
         binding.wq_matmul_noalloc(x, q, s, None, 1, 512, 512, 4, 128, out=out, stream=Stream())
     assert e.value.status == binding.STATUS.index("WQ_ERR_ALIGN")
+
+
+def test_matmul_path_rules(L):
+    # the path is a host decision (no device): few tokens or codes / groups the
+    # tensor-core kernels do not take -> 0; int4 with 64-aligned groups -> 1
+    # (exact); many tokens where rounding w once holds the bound -> 2
+    F16, BF16, F32 = binding.WQ_F16, binding.WQ_BF16, binding.WQ_F32
+    P = binding.wq_matmul_path
+    assert P(16, 8192, 4, 128, BF16, BF16) == 0
+    assert P(64, 8192, 4, 128, BF16, BF16) == 0
+    assert P(65, 8192, 4, 128, BF16, BF16) == 2
+    assert P(4096, 8192, 4, 128, BF16, BF16) == 2
+    assert P(65, 2048, 4, 128, BF16, BF16) == 1     # bf16 below K = 4096: exact path
+    assert P(4096, 512, 4, 128, F16, F16) == 2      # fp16 rounding holds the bound
+    assert P(4096, 8192, 4, 128, F16, BF16) == 1    # scale dtype differs from x
+    assert P(4096, 8192, 4, 32, BF16, BF16) == 0    # group not a multiple of 64
+    assert P(4096, 8192, 2, 64, BF16, BF16) == 0    # int2
+    assert P(64, 4096, 8, -1, BF16, F32) == 0       # int8
+    assert P(100, 4096, 4, -1, BF16, BF16) == 2     # per channel
+    assert P(100, 2048, 4, -1, BF16, BF16) == 1
+    assert P(64, 4096, 3, 128, BF16, BF16) == -1
+    assert P(64, 4096, 4, 48, BF16, BF16) == -1
+    assert P(64, 4096, 8, -1, BF16, BF16) == -1

@@ -38,28 +38,68 @@ def _sweep():
 
 @pytest.mark.parametrize("M", syn.C5_MS)
 def test_prefill_sweep_sampled_rows(M):
+    # every row up to 64 tokens; beyond, 64 sampled rows (first, last, random)
     full, d = _sweep()
     p = full.rows(M)
     dd = dict(d, x=d["x"][:M].contiguous())
     y = run(p, dd).cpu().numpy()
-    rng = np.random.default_rng(M)
-    rows = sorted(set([0, M - 1] + rng.choice(M, size=min(M, 14), replace=False).tolist()))
+    if M <= 64:
+        rows = list(range(M))
+    else:
+        rng = np.random.default_rng(M)
+        rows = sorted(set([0, M - 1] + rng.choice(np.arange(1, M - 1), size=62, replace=False).tolist()))
+        assert len(rows) == 64
     ref = oracle_y(p, rows=rows)
     assert_close(y[rows], ref, p.K, p.name)
     assert np.all(np.isfinite(y))
 
 
-@pytest.mark.parametrize("M", [24, 32, 48])
-def test_decode_several_waves_sampled_rows(M):
-    # 32- and 64-row token tiles on the c5 weights: more CTAs (clusters of K
-    # splits) than the GPU holds at once, so clusters start as others retire.
+@pytest.mark.parametrize("M", [24, 32, 48, 96, 128, 192])
+def test_sweep_weights_mid_m_sampled_rows(M):
+    # the large weights at token counts between the workloads' ones: the
+    # few-token kernel with 32- and 64-row token tiles (several waves of
+    # clusters), the many-token kernel with partial token tiles; called twice
     full, d = _sweep()
     p = full.rows(M)
     dd = dict(d, x=d["x"][:M].contiguous())
     for _ in range(2):
         y = run(p, dd).cpu().numpy()
-        rows = [0, M // 3, M // 2 + 1, M - 1]
+        rows = sorted(set([0, M // 3, M // 2 + 1, M - 1]))
         assert_close(y[rows], oracle_y(p, rows=rows), p.K, p.name)
+
+
+@pytest.mark.parametrize("M", [17, 64, 130])
+def test_sweep_weights_exact_tensor_core_path(M):
+    # the exact tensor-core kernel on the large weights (fp16 x with bf16
+    # scales routes there at any token count above the few-token range;
+    # below it the same call is checked on the few-token kernel)
+    full, _ = _sweep()
+    p = full.rows(M)
+    p = p.__class__(**dict(p.__dict__, x=p.x.to(torch.float16), x_dtype="f16"))
+    want = 0 if M <= 64 else 1
+    assert wq.wq_matmul_path(M, p.K, 4, p.group_size, torch.float16, torch.bfloat16) == want
+    y = run(p).cpu().numpy()
+    rows = sorted(set([0, M // 2, M - 1]))
+    assert_close(y[rows], oracle_y(p, rows=rows), p.K, p.name)
+
+
+SHORT_K = [  # (M, K, N, group, x dtype, symmetric): below K = 4096 the bound is tighter
+    (17, 512, 272, 128, "bf16", False), (65, 1024, 272, 128, "bf16", False), (256, 2048, 384, 64, "bf16", False),
+    (130, 512, 144, 512, "bf16", True), (40, 1024, 128, 256, "f16", False), (256, 512, 272, 128, "f16", False),
+    (300, 1024, 208, 128, "f16", True), (512, 2048, 256, 128, "f16", False), (384, 512, 512, 64, "bf16", False),
+    (100, 512, 64, 64, "bf16", False), (200, 1024, 48, 1024, "bf16", True), (66, 512, 16, 128, "f16", False),
+]
+
+
+@pytest.mark.parametrize("M,K,N,gs,xd,sym", SHORT_K)
+def test_tensor_core_paths_short_k(M, K, N, gs, xd, sym):
+    # bf16 many-token problems below K = 4096 take the exact path (rounding w
+    # to bf16 would not hold the bound there); fp16 ones may round w once.
+    p = syn.grouped("short-k", M, K, N, 4, gs, xd, xd, (0.002, 0.02), symmetric=sym, seed=M + K + N)
+    path = wq.wq_matmul_path(M, K, 4, gs, p.x.dtype, p.scales.dtype)
+    assert path == (0 if M <= 64 else 2 if xd == "f16" else 1)
+    y = run(p).cpu().numpy()
+    assert_close(y, oracle_y(p), K, "short K %s" % ((M, K, N, gs, xd, sym),))
 
 
 INT_EXACT = [  # (name, M, K, N, w_bit, group, x, s, symmetric)
@@ -70,16 +110,28 @@ INT_EXACT = [  # (name, M, K, N, w_bit, group, x, s, symmetric)
     ("int4-asym-bf16-M64", 64, 1024, 512, 4, 128, "bf16", "bf16", False),
     ("int4-perchannel-bf16", 5, 2048, 256, 4, 2048, "bf16", "bf16", False),
     ("int2-g32-f16", 2, 1024, 128, 2, 32, "f16", "bf16", False),
-    # many tokens: the tensor-core (tcgen05) path
+    ("int4-asym-bf16-M24-N400", 24, 2048, 400, 4, 64, "bf16", "bf16", False),
+    ("int4-perchannel-bf16-M40", 40, 1024, 256, 4, 1024, "bf16", "bf16", False),
+    # more tokens: the exact tensor-core path (tcgen05, group scale in fp32) ...
     ("int4-asym-bf16-M200", 200, 1024, 512, 4, 128, "bf16", "bf16", False),
+    ("int4-asym-f16x-bf16s-M70", 70, 1024, 128, 4, 256, "f16", "bf16", False),
+    ("int4-sym-bf16-M100-N272", 100, 2048, 272, 4, 64, "bf16", "bf16", True),
+    # ... and the many-token one (weight rounded once: exact here, scale 2^-4)
     ("int4-sym-f16-M128", 128, 2048, 256, 4, 64, "f16", "f16", True),
     ("int4-asym-f16-M300-N272", 300, 512, 272, 4, 512, "f16", "f16", False),
+    ("int4-asym-bf16-M256-K4096", 256, 4096, 256, 4, 128, "bf16", "bf16", False),
 ]
+
+
+INT_EXACT_PATH = {"int4-asym-bf16-M200": 1, "int4-asym-f16x-bf16s-M70": 1, "int4-sym-bf16-M100-N272": 1,
+                  "int4-sym-f16-M128": 2, "int4-asym-f16-M300-N272": 2, "int4-asym-bf16-M256-K4096": 2}
 
 
 @pytest.mark.parametrize("case", INT_EXACT, ids=[c[0] for c in INT_EXACT])
 def test_integer_exact_bitwise(case):
     name, M, K, N, wb, gs, xd, sd, sym = case
+    dt = {"f16": torch.float16, "bf16": torch.bfloat16}
+    assert wq.wq_matmul_path(M, K, wb, gs, dt[xd], dt[sd]) == INT_EXACT_PATH.get(name, 0)
     p = syn.grouped(name, M, K, N, wb, gs, xd, sd, (0, 0), symmetric=sym, seed=11, int_exact=True)
     y = run(p).cpu().numpy().astype(np.float64)
     ref = oracle_y(p)
@@ -114,10 +166,8 @@ def test_deterministic():
 RAGGED = [  # (M, K, N, w_bit, group) -- tails of token tiles, CTA column blocks, splits, groups
     (3, 256, 80, 4, 64), (13, 512, 48, 4, 128), (17, 1024, 272, 2, 64), (33, 512, 208, 4, 32),
     (7, 4096, 16, 4, 128), (2, 8192, 32, 2, 128), (40, 640, 96, 8, 640), (1, 32, 16, 8, 32), (9, 64, 16, 4, 16),
-    # M > 64 on the tensor-core path: partial 128-token and 256-channel tiles.  K is 4096 here
-    # because that path rounds each weight once to bf16 (relative 2^-9), which the stated
-    # tolerance 1e-2 sqrt(K/4096) RMS absorbs for K >= 4096 but not for small K.
-    (65, 4096, 64, 4, 256), (100, 4096, 144, 4, 128),
+    # M > 16 on the exact tensor-core path: partial token tiles and 128-channel blocks
+    (65, 4096, 64, 4, 256), (100, 4096, 144, 4, 128), (17, 64, 16, 4, 64), (33, 192, 48, 4, 64),
     # M > 64 without a tensor-core path (group 32, int2): 64-row slices of the few-token kernel
     (130, 256, 48, 4, 32), (200, 1024, 64, 2, 64),
 ]

@@ -21,7 +21,9 @@ STATUS = ["WQ_OK", "WQ_ERR_NULL", "WQ_ERR_SHAPE", "WQ_ERR_WBIT", "WQ_ERR_GROUP",
           "WQ_ERR_ALIGN", "WQ_ERR_WORKSPACE", "WQ_ERR_ARCH", "WQ_ERR_CUDA", "WQ_ERR_TIMEOUT"]
 
 EXPORTS = ("wq_status_string", "wq_chunk_k", "wq_packed_bytes", "wq_pack", "wq_unpack",
-           "wq_workspace_bytes", "wq_matmul", "wq_matmul_noalloc", "wq_check_device")
+           "wq_workspace_bytes", "wq_matmul", "wq_matmul_noalloc", "wq_matmul_path", "wq_check_device")
+
+PATHS = {0: "decode_kernel", 1: "midm_kernel", 2: "prefill_kernel"}
 
 
 class WQError(RuntimeError):
@@ -58,6 +60,8 @@ def lib() -> ctypes.CDLL:
         L.wq_matmul.argtypes = [P, I, P, P, I, P, I, I, I, I, I, P, P, Z, P]
         L.wq_matmul_noalloc.restype = I
         L.wq_matmul_noalloc.argtypes = [P, I, P, P, I, P, I, I, I, I, I, P, P]
+        L.wq_matmul_path.restype = I
+        L.wq_matmul_path.argtypes = [I, I, I, I, I, I]
         L.wq_check_device.restype = I
         L.wq_check_device.argtypes = [P]
         _lib = L
@@ -163,6 +167,14 @@ def wq_matmul_noalloc(x: torch.Tensor, packed_w: torch.Tensor, scales: torch.Ten
                                  _ptr(out), _stream(stream))
     _check(st, "wq_matmul_noalloc")
     return out
+
+
+def wq_matmul_path(M: int, K: int, w_bit: int, group_size: int, x_dtype, s_dtype) -> int:
+    """Kernel family wq_matmul runs (0 few-token, 1 exact tensor-core, 2 many-token; -1 invalid).
+    Dtypes are torch dtypes or the WQ_* codes."""
+    xd = _DTYPE.get(x_dtype, x_dtype)
+    sd = _DTYPE.get(s_dtype, s_dtype)
+    return lib().wq_matmul_path(M, K, w_bit, group_size, int(xd), int(sd))
 
 
 def wq_check_device(stream=None) -> None:

@@ -123,14 +123,24 @@ wq_status prepare_call(const void *x, wq_dtype x_dtype, const void *packed_w, co
   a.s_bf16 = (s_dtype == WQ_BF16);
   a.err = d->status;
   c->sms = d->sms;
-  c->prefill = M >= kPrefillMinM && prefill_supported(a);
-  c->need = c->prefill ? 0 : slice_workspace(M, N, K, w_bit, group_size, zeros != nullptr, d->sms);
+  c->route = route_of(a);
+  c->need = c->route == Route::kDecode ? slice_workspace(M, N, K, w_bit, group_size, zeros != nullptr, d->sms) : 0;
   return WQ_OK;
+}
+
+Route route_of(const MatmulArgs &a) {
+  if (a.w_bit != 4 || !midm_supported(a) || a.M <= kDecodeMaxM) return Route::kDecode;
+  if (a.M >= kPrefillMinM && prefill_supported(a) && prefill_within_tolerance(a)) return Route::kPrefill;
+  return Route::kMidm;
 }
 
 wq_status run_call(const Call &c, void *workspace, void *stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (c.prefill) return launch_prefill(c.a, s) == cudaSuccess ? WQ_OK : WQ_ERR_CUDA;
+  if (c.route == Route::kPrefill) return launch_prefill(c.a, s) == cudaSuccess ? WQ_OK : WQ_ERR_CUDA;
+  if (c.route == Route::kMidm) {
+    const MidmPlan pl = plan_midm(c.a.M, c.a.N, c.a.K, c.sms);
+    return launch_midm(c.a, pl, s) == cudaSuccess ? WQ_OK : WQ_ERR_CUDA;
+  }
   // Rows are processed 64 at a time (the few-token kernel's largest token tile).
   MatmulArgs a = c.a;
   const int M = c.a.M, N = a.N, K = a.K;
@@ -204,6 +214,14 @@ size_t wq_workspace_bytes(int M, int N, int K, int w_bit, int group_size) {
   if (device_info(&d) != WQ_OK) return 0;
   if (w_bit == 8 || group_size == -1) group_size = K;
   if (group_size <= 0 || K % group_size != 0) return 0;
+  // The tensor-core paths need no workspace, whatever the dtypes.
+  wq::MatmulArgs a{};
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.w_bit = w_bit;
+  a.group_size = group_size;
+  if (wq::route_of(a) != wq::Route::kDecode) return 0;
   // Enough with zeros or without (the zero rows' shared memory can change the split).
   const size_t with_z = slice_workspace(M, N, K, w_bit, group_size, true, d->sms);
   const size_t without = w_bit == 8 ? with_z : slice_workspace(M, N, K, w_bit, group_size, false, d->sms);
@@ -221,6 +239,31 @@ wq_status wq_matmul(const void *x, wq_dtype x_dtype, const void *packed_w, const
     if (!aligned(workspace, 16)) return WQ_ERR_ALIGN;
   }
   return wq::run_call(c, workspace, stream);
+}
+
+int wq_matmul_path(int M, int K, int w_bit, int group_size, wq_dtype x_dtype, wq_dtype s_dtype) {
+  if (!valid_wbit(w_bit) || M < 0 || K <= 0 || K % (256 / w_bit) != 0) return -1;
+  if (x_dtype != WQ_F16 && x_dtype != WQ_BF16) return -1;
+  wq::MatmulArgs a{};
+  a.M = M;
+  a.K = K;
+  a.w_bit = w_bit;
+  a.x_bf16 = x_dtype == WQ_BF16;
+  if (w_bit == 8) {
+    if (s_dtype != WQ_F32) return -1;
+    a.group_size = K;
+  } else {
+    if (s_dtype != WQ_F16 && s_dtype != WQ_BF16) return -1;
+    a.group_size = group_size == -1 ? K : group_size;
+    if (a.group_size <= 0 || K % a.group_size != 0 || a.group_size % 16 != 0) return -1;
+  }
+  a.s_bf16 = s_dtype == WQ_BF16;
+  switch (wq::route_of(a)) {
+    case wq::Route::kDecode: return 0;
+    case wq::Route::kMidm: return 1;
+    case wq::Route::kPrefill: return 2;
+  }
+  return -1;
 }
 
 wq_status wq_check_device(void *stream) {

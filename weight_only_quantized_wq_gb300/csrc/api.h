@@ -9,13 +9,23 @@
 
 namespace wq {
 
+// Which kernel a call runs on.
+enum class Route {
+  kDecode,   // few tokens, or codes / groups the tensor-core paths do not take (64-token slices)
+  kMidm,     // tensor cores, exact weights, group scale in fp32
+  kPrefill,  // tensor cores, weight rounded once to the x dtype (many tokens)
+};
+
+// Route of a validated call (x and scale dtypes only matter for kPrefill).
+Route route_of(const MatmulArgs &a);
+
 // One validated matmul call: the arguments the kernels take, the route, and
 // the workspace bytes it needs.
 struct Call {
   MatmulArgs a;        // M is the whole call's token count
   int sms = 0;
   bool noop = false;   // M == 0 or N == 0: nothing to do
-  bool prefill = false;
+  Route route = Route::kDecode;
   size_t need = 0;     // workspace bytes (0: none)
 };
 

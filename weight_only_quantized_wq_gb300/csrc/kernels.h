@@ -63,7 +63,34 @@ cudaError_t launch_decode(const MatmulArgs &a, const DecodePlan &p, void *worksp
 bool prefill_supported(const MatmulArgs &a);
 cudaError_t launch_prefill(const MatmulArgs &a, cudaStream_t s);
 
-// Token count from which wq_matmul takes the tensor-core path.
+// Tensor-core path for a moderate number of tokens (int4 codes, group size
+// a multiple of 64): exact weights, group scales applied in fp32.
+struct MidmPlan {
+  int nt;       // tokens per CTA (UMMA N): 16, 32, 64 or 128
+  int mtiles;   // token tiles
+  int nblocks;  // 128-channel blocks
+  int splits;   // K splits (one cluster per channel block and token tile when > 1)
+  int cps;      // 64-wide K stages per split
+};
+bool midm_supported(const MatmulArgs &a);
+MidmPlan plan_midm(int M, int N, int K, int sms);
+cudaError_t launch_midm(const MatmulArgs &a, const MidmPlan &p, cudaStream_t s);
+
+// Most tokens the few-token kernel takes when a tensor-core path can (int4
+// codes, group size a multiple of 64).  Measured on the 8192 x 28672 int4
+// weights: the few-token kernel is the fastest up to 64 tokens, the
+// many-token kernel from 65 on (the exact tensor-core kernel trails both).
+constexpr int kDecodeMaxM = 64;
+// Token count from which the many-token kernel (weight rounded once to the x
+// dtype) takes over; calls it cannot take within the accepted error, or with
+// a scale dtype other than the x dtype, run on the exact tensor-core kernel.
 constexpr int kPrefillMinM = 65;
+// The many-token kernel rounds each dequantized weight once to the x dtype
+// (relative error up to 2^-11 for fp16, 2^-9 for bf16).  Over random signs
+// the result's error stays near that bound / sqrt(3) of the output's RMS, a
+// few times that at the maximum over a large output: within the accepted
+// 1e-2 sqrt(K / 4096) of the RMS for fp16 at any K >= 512, but for bf16 only
+// from K = 4096 on.  Shorter bf16 problems take the exact path.
+inline bool prefill_within_tolerance(const MatmulArgs &a) { return !a.x_bf16 || a.K >= 4096; }
 
 }  // namespace wq

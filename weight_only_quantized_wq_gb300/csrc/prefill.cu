@@ -28,6 +28,7 @@
 #include "dev.cuh"
 #include "kernels.h"
 #include "layout.cuh"
+#include "tc.cuh"
 
 namespace wq {
 
@@ -69,59 +70,6 @@ struct Params {
   int M, N, K, gs, nt_total;
 };
 
-// Shared-memory matrix descriptor of a K-major operand with the 128-byte
-// swizzle: rows of 128 bytes, 8-row atoms 1024 bytes apart.
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
-  uint64_t d = 0;
-  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);  // start address
-  d |= (uint64_t)1 << 16;                     // leading byte offset (unused with this swizzle)
-  d |= (uint64_t)(1024 >> 4) << 32;           // stride byte offset: next 8-row atom
-  d |= (uint64_t)1 << 46;                     // descriptor version
-  d |= (uint64_t)2 << 61;                     // 128-byte swizzle
-  return d;
-}
-
-// Instruction descriptor: fp32 accumulate, A and B both bf16 (or both fp16),
-// both K-major, M = 128, N = 256.
-template <bool BF16>
-__host__ __device__ constexpr uint32_t idesc() {
-  return (1u << 4) | ((BF16 ? 1u : 0u) << 7) | ((BF16 ? 1u : 0u) << 10) | ((uint32_t)(BN >> 3) << 17) |
-         ((uint32_t)(UM >> 4) << 24);
-}
-
-__device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t id, uint32_t acc) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a), "l"(b), "r"(id), "r"(acc)
-      : "memory");
-}
-
-__device__ __forceinline__ void umma_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-// Byte offset of element (row r, k) of a K-major 128-byte-swizzled bf16 tile.
-__device__ __forceinline__ uint32_t sw128_off(int r, int k) {
-  return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((((k * 2) >> 4) ^ (r & 7)) << 4) + ((k * 2) & 15));
-}
-
-__device__ __forceinline__ void sts64u(uint32_t a, uint32_t x, uint32_t y) {
-  asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(a), "r"(x), "r"(y) : "memory");
-}
-
-template <bool BF16>
-__device__ __forceinline__ uint32_t sub2(uint32_t a, uint32_t b) {
-  uint32_t d;
-  if constexpr (BF16)
-    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-  else
-    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-  return d;
-}
 template <bool BF16>
 __device__ __forceinline__ uint32_t mul2(uint32_t a, uint32_t b) {
   uint32_t d;
@@ -135,16 +83,8 @@ __device__ __forceinline__ uint32_t mul2(uint32_t a, uint32_t b) {
 // 32 consecutive fp32 columns of this warp's TMEM lane quarter.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   uint32_t r[32];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%"
-      "28,%29,%30,%31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
-        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
-        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+  tc::ld32(taddr, r);
+  tc::wait_ld();
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
@@ -190,14 +130,11 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
     fence_barrier_init();
   }
   if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(tmem_slot)),
-                 "r"(TMEM_COLS)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    tc::alloc(smem_addr(tmem_slot), TMEM_COLS);
   }
-  tc_fence_before();
+  tc::fence_before();
   __syncthreads();
-  tc_fence_after();
+  tc::fence_after();
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
@@ -224,24 +161,24 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t id = idesc<BF16>();
+      constexpr uint32_t id = tc::idesc<BF16>(UM, BN);
       for (int i = 0; i < nk; ++i) {
         const int st = i % STAGES, sb = i % BSTAGES;
         if (!mbar_wait(smem_addr(&full[st]), (i / STAGES) & 1, p.err, abort_flag)) break;
         if (!mbar_wait(smem_addr(&bfull[sb]), (i / BSTAGES) & 1, p.err, abort_flag)) break;
-        tc_fence_after();
+        tc::fence_after();
         const uint32_t a0 = smem_addr(ring + st * STAGE_BYTES + ST_A);
         const uint32_t b0 = smem_addr(bbuf + sb * B_BYTES);
 #pragma unroll
         for (int h = 0; h < MSUB; ++h)
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk)
-            umma(tmem + h * BN, sw128_desc(a0 + h * (UM * 128) + kk * 32), sw128_desc(b0 + kk * 32), id,
+            tc::mma(tmem + h * BN, tc::sw128_desc(a0 + h * (UM * 128) + kk * 32), tc::sw128_desc(b0 + kk * 32), id,
                  (i | kk) != 0);
-        umma_commit(smem_addr(&empty[st]));
-        umma_commit(smem_addr(&bempty[sb]));
+        tc::commit(smem_addr(&empty[st]));
+        tc::commit(smem_addr(&bempty[sb]));
       }
-      umma_commit(smem_addr(accfull));  // every MMA issued above has completed when this fires
+      tc::commit(smem_addr(accfull));  // every MMA issued above has completed when this fires
     }
   } else {
     // ------------------------------------------------------------ dequant (warps 2..9)
@@ -275,10 +212,10 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
               const uint32_t w = w4[2 * u + r];
 #pragma unroll
               for (int j = 0; j < 2; ++j) {
-                const uint32_t lo = mul2<BF16>(sub2<BF16>(code_pair<4, BF16>(w, 2 * j), zz), ss);
-                const uint32_t hi = mul2<BF16>(sub2<BF16>(code_pair<4, BF16>(w, 2 * j + 1), zz), ss);
+                const uint32_t lo = mul2<BF16>(sub_pair<BF16>(code_pair<4, BF16>(w, 2 * j), zz), ss);
+                const uint32_t hi = mul2<BF16>(sub_pair<BF16>(code_pair<4, BF16>(w, 2 * j + 1), zz), ss);
                 const int k = 32 * u + 16 * j + 4 * tq;
-                sts64u(bdst + sw128_off(col, k), lo, hi);
+                sts64(bdst + tc::sw128_off(col, k), lo, hi);
               }
             }
           }
@@ -292,7 +229,7 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
     if (warp >= 4 && warp < 8) {
       const int q = warp & 3;  // TMEM lane quarter this warp may access
       mbar_wait(smem_addr(accfull), 0, p.err, nullptr);
-      tc_fence_after();
+      tc::fence_after();
       for (int h = 0; h < MSUB; ++h) {
         const int m = m0 + h * UM + q * 32 + lane;
         for (int c = 0; c < BN; c += 32) {
@@ -314,11 +251,11 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
       }
     }
   }
-  tc_fence_before();
+  tc::fence_before();
   __syncthreads();
   if (warp == 1) {
-    tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
+    tc::fence_after();
+    tc::dealloc(tmem, TMEM_COLS);
   }
 }
 
