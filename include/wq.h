@@ -181,6 +181,23 @@ WQ_API wq_status wq_matmul(const void *x, wq_dtype x_dtype, const void *packed_w
                     float *out, void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * wq_matmul_ex -- wq_matmul with a choice of output element type.
+ *
+ * out (M, N) row-major of out_dtype: WQ_F32 (the same as wq_matmul), WQ_F16
+ * or WQ_BF16.  The result is accumulated in fp32 exactly as for wq_matmul and
+ * rounded once, to nearest even, when it is stored: the fp16 output of
+ * Marlin's write_result (aphrodite-engine marlin_cuda_kernel.cu, C allocated
+ * in the activation dtype by marlin_gemm), without its fp16 reduction buffer.
+ * A 16-bit output halves the bytes the epilogue writes.  Any other out_dtype
+ * is WQ_ERR_DTYPE.  Every other argument, requirement and status as wq_matmul.
+ */
+WQ_API wq_status wq_matmul_ex(const void *x, wq_dtype x_dtype, const void *packed_w,
+                              const void *scales, wq_dtype s_dtype, const int32_t *zeros,
+                              int M, int N, int K, int w_bit, int group_size,
+                              void *out, wq_dtype out_dtype,
+                              void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * wq_matmul_noalloc -- wq_matmul for callers that cannot allocate device memory.
  *
  * The pages have no counterpart to this entry point.  It exists for callers

@@ -60,6 +60,21 @@ def _mm(L, **kw):
                        a["out"], a["ws"], a["wsb"], None)
 
 
+def test_matmul_ex_host_validation(L):
+    S = {n: i for i, n in enumerate(binding.STATUS)}
+
+    def mx(odt, **kw):
+        a = dict(x=FAKE, xd=1, w=FAKE, s=FAKE, sd=1, z=None, M=4, N=64, K=128, wb=4, gs=64, out=FAKE + 8)
+        a.update(kw)
+        return L.wq_matmul_ex(a["x"], a["xd"], a["w"], a["s"], a["sd"], a["z"], a["M"], a["N"], a["K"], a["wb"],
+                              a["gs"], a["out"], odt, None, 0, None)
+    assert mx(3) == S["WQ_ERR_DTYPE"]      # no such output type
+    assert mx(-1) == S["WQ_ERR_DTYPE"]
+    assert mx(0) == S["WQ_ERR_ALIGN"]      # a valid type reaches the alignment check (out misaligned)
+    assert mx(1, out=None) == S["WQ_ERR_NULL"]
+    assert mx(1, M=0) == S["WQ_OK"]
+
+
 def test_matmul_host_validation(L):
     S = {n: i for i, n in enumerate(binding.STATUS)}
     assert _mm(L, x=None) == S["WQ_ERR_NULL"]

@@ -21,7 +21,8 @@ STATUS = ["WQ_OK", "WQ_ERR_NULL", "WQ_ERR_SHAPE", "WQ_ERR_WBIT", "WQ_ERR_GROUP",
           "WQ_ERR_ALIGN", "WQ_ERR_WORKSPACE", "WQ_ERR_ARCH", "WQ_ERR_CUDA", "WQ_ERR_TIMEOUT"]
 
 EXPORTS = ("wq_status_string", "wq_chunk_k", "wq_packed_bytes", "wq_pack", "wq_unpack",
-           "wq_workspace_bytes", "wq_matmul", "wq_matmul_noalloc", "wq_matmul_path", "wq_check_device")
+           "wq_workspace_bytes", "wq_matmul", "wq_matmul_ex", "wq_matmul_noalloc", "wq_matmul_path",
+           "wq_check_device")
 
 PATHS = {0: "decode_kernel", 1: "midm_kernel", 2: "prefill_kernel"}
 
@@ -58,6 +59,8 @@ def lib() -> ctypes.CDLL:
         L.wq_workspace_bytes.argtypes = [I, I, I, I, I]
         L.wq_matmul.restype = I
         L.wq_matmul.argtypes = [P, I, P, P, I, P, I, I, I, I, I, P, P, Z, P]
+        L.wq_matmul_ex.restype = I
+        L.wq_matmul_ex.argtypes = [P, I, P, P, I, P, I, I, I, I, I, P, I, P, Z, P]
         L.wq_matmul_noalloc.restype = I
         L.wq_matmul_noalloc.argtypes = [P, I, P, P, I, P, I, I, I, I, I, P, P]
         L.wq_matmul_path.restype = I
@@ -152,6 +155,23 @@ def wq_matmul(x: torch.Tensor, packed_w: torch.Tensor, scales: torch.Tensor, zer
                          _DTYPE.get(scales.dtype, -1), _ptr(zeros), M, N, K, w_bit, group_size,
                          _ptr(out), _ptr(workspace), ws_bytes, _stream(stream))
     _check(st, "wq_matmul")
+    return out
+
+
+def wq_matmul_ex(x: torch.Tensor, packed_w: torch.Tensor, scales: torch.Tensor, zeros: torch.Tensor | None,
+                 M: int, N: int, K: int, w_bit: int, group_size: int, out: torch.Tensor | None = None,
+                 out_dtype=torch.float32, workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """y (M, N) in out_dtype (fp32, fp16 or bf16) = x @ dequant(W), accumulated in fp32 and
+    rounded once on store, through the C entry point wq_matmul_ex."""
+    if out is None:
+        out = torch.empty((M, N), dtype=out_dtype, device=x.device)
+    if workspace is None:
+        workspace = workspace_for(M, N, K, w_bit, group_size, x.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib().wq_matmul_ex(_ptr(x), _DTYPE.get(x.dtype, -1), _ptr(packed_w), _ptr(scales),
+                            _DTYPE.get(scales.dtype, -1), _ptr(zeros), M, N, K, w_bit, group_size,
+                            _ptr(out), _DTYPE.get(out.dtype, -1), _ptr(workspace), ws_bytes, _stream(stream))
+    _check(st, "wq_matmul_ex")
     return out
 
 

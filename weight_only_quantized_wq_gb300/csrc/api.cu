@@ -84,7 +84,8 @@ size_t slice_workspace(int M, int N, int K, int w_bit, int group_size, bool zero
 namespace wq {
 
 wq_status prepare_call(const void *x, wq_dtype x_dtype, const void *packed_w, const void *scales, wq_dtype s_dtype,
-                       const int32_t *zeros, int M, int N, int K, int w_bit, int group_size, float *out, Call *c) {
+                       const int32_t *zeros, int M, int N, int K, int w_bit, int group_size, void *out,
+                       wq_dtype out_dtype, Call *c) {
   *c = Call{};
   if (!x || !packed_w || !scales || !out) return WQ_ERR_NULL;
   if (!valid_wbit(w_bit)) return WQ_ERR_WBIT;
@@ -96,6 +97,7 @@ wq_status prepare_call(const void *x, wq_dtype x_dtype, const void *packed_w, co
   wq_status st = check_kn(K, N, w_bit);
   if (st != WQ_OK) return st;
   if (x_dtype != WQ_F16 && x_dtype != WQ_BF16) return WQ_ERR_DTYPE;
+  if (out_dtype != WQ_F32 && out_dtype != WQ_F16 && out_dtype != WQ_BF16) return WQ_ERR_DTYPE;
   if (w_bit == 8) {
     if (s_dtype != WQ_F32 || zeros != nullptr) return WQ_ERR_DTYPE;
     group_size = K;
@@ -114,6 +116,7 @@ wq_status prepare_call(const void *x, wq_dtype x_dtype, const void *packed_w, co
   a.scales = scales;
   a.zeros = reinterpret_cast<const uint32_t *>(zeros);
   a.out = out;
+  a.out_type = out_dtype == WQ_F32 ? kOutF32 : out_dtype == WQ_F16 ? kOutF16 : kOutBF16;
   a.M = M;
   a.N = N;
   a.K = K;
@@ -149,7 +152,7 @@ wq_status run_call(const Call &c, void *workspace, void *stream) {
   for (int m0 = 0; m0 < M; m0 += 64) {
     a.M = (M - m0) < 64 ? (M - m0) : 64;
     a.x = static_cast<const uint16_t *>(c.a.x) + (size_t)m0 * K;
-    a.out = c.a.out + (size_t)m0 * N;
+    a.out = static_cast<char *>(c.a.out) + (size_t)m0 * N * (a.out_type == kOutF32 ? 4 : 2);
     const DecodePlan p = (a.M == (M < 64 ? M : 64)) ? full : plan_decode(a.M, N, K, a.w_bit, a.group_size, zero, c.sms);
     if (launch_decode(a, p, workspace, s) != cudaSuccess) return WQ_ERR_CUDA;
   }
@@ -228,17 +231,25 @@ size_t wq_workspace_bytes(int M, int N, int K, int w_bit, int group_size) {
   return with_z > without ? with_z : without;
 }
 
-wq_status wq_matmul(const void *x, wq_dtype x_dtype, const void *packed_w, const void *scales, wq_dtype s_dtype,
-                    const int32_t *zeros, int M, int N, int K, int w_bit, int group_size, float *out,
-                    void *workspace, size_t workspace_bytes, void *stream) {
+wq_status wq_matmul_ex(const void *x, wq_dtype x_dtype, const void *packed_w, const void *scales, wq_dtype s_dtype,
+                       const int32_t *zeros, int M, int N, int K, int w_bit, int group_size, void *out,
+                       wq_dtype out_dtype, void *workspace, size_t workspace_bytes, void *stream) {
   wq::Call c;
-  wq_status st = wq::prepare_call(x, x_dtype, packed_w, scales, s_dtype, zeros, M, N, K, w_bit, group_size, out, &c);
+  wq_status st = wq::prepare_call(x, x_dtype, packed_w, scales, s_dtype, zeros, M, N, K, w_bit, group_size, out,
+                                  out_dtype, &c);
   if (st != WQ_OK || c.noop) return st;
   if (c.need > 0) {
     if (!workspace || workspace_bytes < c.need) return WQ_ERR_WORKSPACE;
     if (!aligned(workspace, 16)) return WQ_ERR_ALIGN;
   }
   return wq::run_call(c, workspace, stream);
+}
+
+wq_status wq_matmul(const void *x, wq_dtype x_dtype, const void *packed_w, const void *scales, wq_dtype s_dtype,
+                    const int32_t *zeros, int M, int N, int K, int w_bit, int group_size, float *out,
+                    void *workspace, size_t workspace_bytes, void *stream) {
+  return wq_matmul_ex(x, x_dtype, packed_w, scales, s_dtype, zeros, M, N, K, w_bit, group_size, out, WQ_F32,
+                      workspace, workspace_bytes, stream);
 }
 
 int wq_matmul_path(int M, int K, int w_bit, int group_size, wq_dtype x_dtype, wq_dtype s_dtype) {

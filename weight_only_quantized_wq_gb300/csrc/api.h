@@ -32,7 +32,8 @@ struct Call {
 // Every host check of wq_matmul, in order, before anything touches a device
 // (the device query comes last).  Fills *c on WQ_OK.
 wq_status prepare_call(const void *x, wq_dtype x_dtype, const void *packed_w, const void *scales, wq_dtype s_dtype,
-                       const int32_t *zeros, int M, int N, int K, int w_bit, int group_size, float *out, Call *c);
+                       const int32_t *zeros, int M, int N, int K, int w_bit, int group_size, void *out,
+                       wq_dtype out_dtype, Call *c);
 
 // Enqueue the kernels of a prepared call on `stream`; workspace holds at
 // least c.need bytes (zero-filled counters) when c.need > 0.

@@ -180,6 +180,7 @@ cudaError_t launch_decode(const MatmulArgs &a, const DecodePlan &p, void *worksp
   dp.scales = a.scales;
   dp.zeros = a.zeros;
   dp.out = a.out;
+  dp.out_type = a.out_type;
   dp.M = a.M;
   dp.N = a.N;
   dp.K = a.K;

@@ -100,7 +100,8 @@ struct DecodeParams {
   const uint8_t *packed;
   const void *scales;     // (G, N) 16-bit, or (N,) fp32 for int8
   const uint32_t *zeros;  // (ceil(G / V), N) or nullptr
-  float *out;
+  void *out;
+  int out_type;  // OutType
   float *partial;
   int *counters;
   uint32_t *err;
@@ -413,13 +414,16 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_min_blocks(MT, TN))
         v.z *= s4.z;
         v.w *= s4.w;
       }
-      *reinterpret_cast<float4 *>(p.out + (size_t)m * p.N + n0 + col) = v;
+      store_out4(p.out, (size_t)m * p.N + n0 + col, v, p.out_type);
     }
     __syncwarp();
     cluster_sync_relaxed();  // no CTA leaves while another still reads its shared memory
     return;
   }
-  float *dst = p.splits == 1 ? p.out : p.partial + (size_t)split * p.M * p.N;
+  // One split: the result itself (in the output type); more: this split's
+  // fp32 partial in the workspace.
+  void *dst = p.splits == 1 ? p.out : static_cast<void *>(p.partial + (size_t)split * p.M * p.N);
+  const int dst_type = p.splits == 1 ? p.out_type : kOutF32;
 #pragma unroll
   for (int ti = 0; ti < TN; ++ti) {
     if (wt0 + ti >= ntiles) continue;
@@ -432,7 +436,7 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_min_blocks(MT, TN))
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           const int m = mt * 8 + 2 * t + c;
-          if (m < p.M) dst[(size_t)m * p.N + n] = acc[ti][mt][2 * rr + c] * s8;
+          if (m < p.M) store_out1(dst, (size_t)m * p.N + n, acc[ti][mt][2 * rr + c] * s8, dst_type);
         }
     }
   }
@@ -472,7 +476,7 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_min_blocks(MT, TN))
       v.z *= s4.z;
       v.w *= s4.w;
     }
-    *reinterpret_cast<float4 *>(p.out + (size_t)m * p.N + n) = v;
+    store_out4(p.out, (size_t)m * p.N + n, v, p.out_type);
   }
   if (threadIdx.x == 0) p.counters[nb] = 0;
 }

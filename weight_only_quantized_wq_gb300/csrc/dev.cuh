@@ -6,7 +6,11 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
+
+#include "kernels.h"
 
 namespace wq {
 
@@ -296,6 +300,31 @@ __device__ __forceinline__ uint32_t int8_pair(uint32_t w, int hi_half) {
     asm("sub.f16x2 %0, %1, %2;" : "=r"(r) : "r"(h), "r"(0x64806480u));
     return r;
   }
+}
+
+// ---------------------------------------------------------------- output
+// out[idx .. idx + 3] = v (idx a multiple of 4; out 16-byte aligned).
+__device__ __forceinline__ void store_out4(void *out, size_t idx, float4 v, int ot) {
+  if (ot == kOutF32) {
+    *reinterpret_cast<float4 *>(static_cast<float *>(out) + idx) = v;
+  } else if (ot == kOutF16) {
+    __half2 a = __floats2half2_rn(v.x, v.y), b = __floats2half2_rn(v.z, v.w);
+    *reinterpret_cast<uint2 *>(static_cast<__half *>(out) + idx) =
+        make_uint2(*reinterpret_cast<uint32_t *>(&a), *reinterpret_cast<uint32_t *>(&b));
+  } else {
+    __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
+    *reinterpret_cast<uint2 *>(static_cast<__nv_bfloat16 *>(out) + idx) =
+        make_uint2(*reinterpret_cast<uint32_t *>(&a), *reinterpret_cast<uint32_t *>(&b));
+  }
+}
+// out[idx] = v.
+__device__ __forceinline__ void store_out1(void *out, size_t idx, float v, int ot) {
+  if (ot == kOutF32)
+    static_cast<float *>(out)[idx] = v;
+  else if (ot == kOutF16)
+    static_cast<__half *>(out)[idx] = __float2half_rn(v);
+  else
+    static_cast<__nv_bfloat16 *>(out)[idx] = __float2bfloat16_rn(v);
 }
 
 __device__ __forceinline__ float half_bits_to_float(uint16_t h, bool bf16) {

@@ -18,13 +18,18 @@ bool encode_2d(CUtensorMap *m, const void *base, int elem_bytes, uint64_t cols, 
 cudaError_t launch_pack(const void *qin, void *out, int K, int N, int w_bit, cudaStream_t s);
 cudaError_t launch_unpack(const void *packed, uint8_t *codes, int K, int N, int w_bit, cudaStream_t s);
 
+// Output element types of the matmul epilogues: the fp32 result is stored as
+// is or rounded once (to nearest even) to fp16 or bf16.
+enum OutType : int { kOutF32 = 0, kOutF16 = 1, kOutBF16 = 2 };
+
 // Problem handed to the matmul kernels after host validation.
 struct MatmulArgs {
   const void *x;          // (M, K) f16/bf16
   const void *packed;     // wq_pack layout
   const void *scales;     // (G, N) f16/bf16, or (N,) f32 for int8
   const uint32_t *zeros;  // (ceil(G/V), N) or nullptr
-  float *out;             // (M, N)
+  void *out;              // (M, N), element type out_type
+  int out_type;           // OutType: fp32, fp16 or bf16
   int M, N, K, w_bit, group_size;
   bool x_bf16, s_bf16;
   uint32_t *err;          // device status word

@@ -78,7 +78,8 @@ struct Params {
   CUtensorMap tm_s;  // scales (G, N) 16-bit, box (128, 1)
   CUtensorMap tm_z;  // zero words (ceil(G/8), N) 32-bit, box (128, 1)
   const uint8_t *packed;
-  float *out;
+  void *out;
+  int out_type;  // OutType
   uint32_t *err;
   int M, N, K, gs, nt_total, kch, cps, splits;
   bool s_bf16;
@@ -375,7 +376,7 @@ __global__ void __launch_bounds__(THREADS, midm_min_blocks(NT)) midm_kernel(cons
             v.w += u[j].w;
           }
       }
-      *reinterpret_cast<float4 *>(p.out + (size_t)(m0 + m) * p.N + n0 + c4) = v;
+      store_out4(p.out, (size_t)(m0 + m) * p.N + n0 + c4, v, p.out_type);
     }
     __syncwarp();
     cluster_sync_relaxed();  // no CTA leaves while another still reads its shared memory
@@ -383,8 +384,8 @@ __global__ void __launch_bounds__(THREADS, midm_min_blocks(NT)) midm_kernel(cons
     const float *redp = reinterpret_cast<const float *>(xring);
     for (int qd = threadIdx.x; qd < rows * qpr; qd += THREADS) {
       const int m = qd / qpr, c4 = (qd % qpr) * 4;
-      *reinterpret_cast<float4 *>(p.out + (size_t)(m0 + m) * p.N + n0 + c4) =
-          *reinterpret_cast<const float4 *>(redp + m * C::RP + c4);
+      store_out4(p.out, (size_t)(m0 + m) * p.N + n0 + c4, *reinterpret_cast<const float4 *>(redp + m * C::RP + c4),
+                 p.out_type);
     }
   }
   if (warp == 1) {
@@ -550,6 +551,7 @@ cudaError_t launch_midm(const MatmulArgs &a, const MidmPlan &pl, cudaStream_t s)
     return cudaErrorInvalidValue;
   pp.packed = static_cast<const uint8_t *>(a.packed);
   pp.out = a.out;
+  pp.out_type = a.out_type;
   pp.err = a.err;
   pp.M = a.M;
   pp.N = a.N;

@@ -55,7 +55,8 @@ wq_status wq_matmul_noalloc(const void *x, wq_dtype x_dtype, const void *packed_
                             float *out, void *stream) {
   // Every argument check runs first: an invalid call enqueues nothing.
   wq::Call c;
-  wq_status st = wq::prepare_call(x, x_dtype, packed_w, scales, s_dtype, zeros, M, N, K, w_bit, group_size, out, &c);
+  wq_status st =
+      wq::prepare_call(x, x_dtype, packed_w, scales, s_dtype, zeros, M, N, K, w_bit, group_size, out, WQ_F32, &c);
   if (st != WQ_OK || c.noop) return st;
   if (c.need > kNoAllocScratchBytes) return WQ_ERR_WORKSPACE;
   void *scratch = nullptr;

@@ -65,7 +65,8 @@ struct Params {
   CUtensorMap tm_s;  // scales (G, N) 16-bit, box (256, 1)
   CUtensorMap tm_z;  // zeros (ceil(G/8), N) 32-bit, box (256, 1)
   const uint8_t *packed;
-  float *out;
+  void *out;
+  int out_type;  // OutType
   uint32_t *err;
   int M, N, K, gs, nt_total;
 };
@@ -236,15 +237,15 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
           float v[32];
           tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + h * BN + c, v);
           if (m < p.M) {
-            float *dst = p.out + (size_t)m * p.N + n0 + c;
+            const size_t row = (size_t)m * p.N + n0 + c;
             if (n0 + c + 32 <= p.N) {
 #pragma unroll
               for (int j = 0; j < 32; j += 4)
-                *reinterpret_cast<float4 *>(dst + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+                store_out4(p.out, row + j, make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]), p.out_type);
             } else {
 #pragma unroll
               for (int j = 0; j < 32; ++j)
-                if (n0 + c + j < p.N) dst[j] = v[j];
+                if (n0 + c + j < p.N) store_out1(p.out, row + j, v[j], p.out_type);
             }
           }
         }
@@ -303,6 +304,7 @@ cudaError_t launch_prefill(const MatmulArgs &a, cudaStream_t s) {
     return cudaErrorInvalidValue;
   pp.packed = static_cast<const uint8_t *>(a.packed);
   pp.out = a.out;
+  pp.out_type = a.out_type;
   pp.err = a.err;
   pp.M = a.M;
   pp.N = a.N;
