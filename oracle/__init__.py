@@ -50,8 +50,12 @@ def _bind(path: str):
     lib.wq_oracle_dequant.argtypes = [P, P, I, P, I, I, I, I, P]
     lib.wq_oracle_matmul_grouped.argtypes = [P, I, P, P, I, P, I, I, I, I, I, I, I, P, I, P]
     lib.wq_oracle_matmul_int8.argtypes = [P, I, P, P, I, I, I, I, I, P, I, P]
+    lib.wq_oracle_t2_unpack.argtypes = [P, I, I, P]
+    lib.wq_oracle_t2_pack.argtypes = [P, I, I, P]
+    lib.wq_oracle_t2_matmul.argtypes = [P, P, I, I, I, P]
     for f in ("wq_oracle_decode16_array", "wq_oracle_unpack", "wq_oracle_pack",
-              "wq_oracle_dequant", "wq_oracle_matmul_grouped", "wq_oracle_matmul_int8"):
+              "wq_oracle_dequant", "wq_oracle_matmul_grouped", "wq_oracle_matmul_int8",
+              "wq_oracle_t2_unpack", "wq_oracle_t2_pack", "wq_oracle_t2_matmul"):
         getattr(lib, f).restype = I
     return lib
 
@@ -161,6 +165,36 @@ class Oracle:
                                              _ptr(r), nr, _ptr(y)), "matmul_int8")
         return y
 
+    def t2_unpack(self, packed, K: int, N: int) -> np.ndarray:
+        """Liger planar 2-bit bytes (K/4, N) -> int8 weights (K, N) in {-1, 0, 1, 2}
+        (Liger ops/experimental/mm_int8int2.py, unpack_weights)."""
+        packed = np.ascontiguousarray(_np(packed), dtype=np.uint8)
+        w = np.empty((K, N), dtype=np.int8)
+        _check(self._lib.wq_oracle_t2_unpack(_ptr(packed), K, N, _ptr(w)), "t2_unpack")
+        return w
+
+    def t2_pack(self, w) -> np.ndarray:
+        """int8 weights (K, N) in {-1, 0, 1, 2} -> planar bytes (K/4, N) (pack_weights)."""
+        w = np.ascontiguousarray(_np(w), dtype=np.int8)
+        K, N = w.shape
+        packed = np.empty((K // 4, N), dtype=np.uint8)
+        _check(self._lib.wq_oracle_t2_pack(_ptr(w), K, N, _ptr(packed)), "t2_pack")
+        return packed
+
+    def t2_matmul(self, x, packed, M: int, N: int, K: int) -> np.ndarray:
+        """int64 y = x (M, K) int8 @ unpacked ternary weights (Liger matmul_kernel, exact)."""
+        x = np.ascontiguousarray(_np(x), dtype=np.int8)
+        packed = np.ascontiguousarray(_np(packed), dtype=np.uint8)
+        y = np.empty((M, N), dtype=np.int64)
+        _check(self._lib.wq_oracle_t2_matmul(_ptr(x), _ptr(packed), M, N, K, _ptr(y)), "t2_matmul")
+        return y
+
+
+def _np(a):
+    if "torch" in type(a).__module__:
+        return a.detach().cpu().contiguous().numpy()
+    return a
+
 
 def load(path: str | None = None) -> Oracle:
     """The oracle bound to the default build (path None) or to another compiled copy."""
@@ -184,3 +218,6 @@ def pack(*a, **k): return _get().pack(*a, **k)
 def dequant(*a, **k): return _get().dequant(*a, **k)
 def matmul_grouped(*a, **k): return _get().matmul_grouped(*a, **k)
 def matmul_int8(*a, **k): return _get().matmul_int8(*a, **k)
+def t2_unpack(*a, **k): return _get().t2_unpack(*a, **k)
+def t2_pack(*a, **k): return _get().t2_pack(*a, **k)
+def t2_matmul(*a, **k): return _get().t2_matmul(*a, **k)

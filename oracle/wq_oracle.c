@@ -250,3 +250,58 @@ int wq_oracle_matmul_int8(const uint16_t *x, int x_is_bf16, const int8_t *q,
     }
     return 0;
 }
+
+/*
+ * Liger kernels, ops/experimental/mm_int8int2.py (page 1): ternary weights in
+ * {-1, 0, 1} stored plus one as 2-bit fields of uint8, planar along K.
+ * pack_weights / unpack_weights: with R = K / 4 rows of bytes (K % 4 == 0
+ * here), plane i = 0..3 holds rows k = i R .. i R + R - 1 in bits 2i, 2i+1
+ * of byte [k - i R][n], i.e. for any k:
+ *   w(k, n) = ((packed[k mod R][n] >> (2 (k div R))) & 3) - 1.
+ * matmul_kernel: C = A (M, K) int8 times w (K, N), accumulated in int32.
+ * Here the sum is exact in int64 (the caller checks it fits int32).
+ */
+static int t2_value(const uint8_t *packed, int K, int N, int k, int n)
+{
+    int R = K / 4;
+    return (int)((packed[(size_t)(k % R) * N + n] >> (2 * (k / R))) & 3u) - 1;
+}
+
+/* Planar packed bytes (K/4, N) -> weights (K, N) as int8 in {-1, 0, 1, 2}. */
+int wq_oracle_t2_unpack(const uint8_t *packed, int K, int N, int8_t *w)
+{
+    if (!packed || !w || K <= 0 || N < 0 || K % 4) return -1;
+    for (int k = 0; k < K; ++k)
+        for (int n = 0; n < N; ++n)
+            w[(size_t)k * N + n] = (int8_t)t2_value(packed, K, N, k, n);
+    return 0;
+}
+
+/* Inverse: weights (K, N) in {-1, 0, 1, 2} -> planar packed bytes (K/4, N). */
+int wq_oracle_t2_pack(const int8_t *w, int K, int N, uint8_t *packed)
+{
+    if (!packed || !w || K <= 0 || N < 0 || K % 4) return -1;
+    int R = K / 4;
+    for (size_t i = 0; i < (size_t)R * N; ++i) packed[i] = 0;
+    for (int k = 0; k < K; ++k)
+        for (int n = 0; n < N; ++n) {
+            int v = w[(size_t)k * N + n] + 1;
+            if (v < 0 || v > 3) return -1;
+            packed[(size_t)(k % R) * N + n] |= (uint8_t)(v << (2 * (k / R)));
+        }
+    return 0;
+}
+
+/* y (M, N) int64 = x (M, K) int8 times the unpacked weights, k ascending. */
+int wq_oracle_t2_matmul(const int8_t *x, const uint8_t *packed, int M, int N, int K, int64_t *y)
+{
+    if (!x || !packed || !y || M < 0 || N < 0 || K <= 0 || K % 4) return -1;
+    for (int m = 0; m < M; ++m)
+        for (int n = 0; n < N; ++n) {
+            int64_t acc = 0;
+            for (int k = 0; k < K; ++k)
+                acc += (int64_t)x[(size_t)m * K + k] * (int64_t)t2_value(packed, K, N, k, n);
+            y[(size_t)m * N + n] = acc;
+        }
+    return 0;
+}

@@ -30,7 +30,15 @@ def pin_golden(orc):
     """Hand-worked values for unpacking, zeros, and tiny matmuls."""
     cases = json.load(open(GOLDEN))["cases"]
     for c in cases:
-        if "codes" in c:
+        if c.get("t2"):
+            packed = np.array(c["packed"], dtype=np.uint8).reshape(c["K"] // 4, c["N"])
+            w = orc.t2_unpack(packed, c["K"], c["N"])
+            assert w.ravel().tolist() == c["w"], (c["id"], w)
+            assert np.array_equal(orc.t2_pack(w), packed), c["id"]
+            x = np.array(c["x"], dtype=np.int8).reshape(c["M"], c["K"])
+            y = orc.t2_matmul(x, packed, c["M"], c["N"], c["K"])
+            assert y.ravel().tolist() == c["y"], (c["id"], y)
+        elif "codes" in c:
             pk = 32 // c["w_bit"]
             qw = _hexwords(c["qweight_hex"], (c["K"] + pk - 1) // pk, c["N"])
             got = orc.unpack(qw, c["K"], c["N"], c["w_bit"]).ravel().tolist()
@@ -226,6 +234,32 @@ def pin_dequant_closed_form(orc):
                 assert np.array_equal(y[0], got[k]), (wb, k)
 
 
+def pin_t2_numpy(orc):
+    """Ternary planar int2: bytes built with numpy shifts from weights the test
+    drew (plane k // R in bits 2 (k // R), row k % R) unpack to those weights;
+    the matmul equals numpy's int64 x @ w; pack and unpack are inverse (also on
+    random bytes, whose field 3 stands for 2)."""
+    rng = np.random.default_rng(9)
+    for K, N, M in ((8, 3, 2), (64, 5, 3), (256, 7, 4)):
+        R = K // 4
+        w = rng.integers(-1, 2, (K, N)).astype(np.int8)
+        packed = np.zeros((R, N), dtype=np.uint8)
+        for k in range(K):
+            packed[k % R] |= ((w[k] + 1).astype(np.uint8) << np.uint8(2 * (k // R)))
+        assert np.array_equal(orc.t2_unpack(packed, K, N), w), K
+        x = rng.integers(-128, 128, (M, K)).astype(np.int8)
+        ref = x.astype(np.int64) @ w.astype(np.int64)
+        assert np.array_equal(orc.t2_matmul(x, packed, M, N, K), ref), K
+        assert np.array_equal(orc.t2_pack(w), packed), K
+        raw = rng.integers(0, 256, (R, N)).astype(np.uint8)
+        assert np.array_equal(orc.t2_pack(orc.t2_unpack(raw, K, N)), raw), K
+    # extremes: every weight 2 (field 3) and x = -128 over K = 4096: -128 * 2 * 4096
+    K = 4096
+    packed = np.full((K // 4, 2), 0xFF, dtype=np.uint8)
+    x = np.full((1, K), -128, dtype=np.int8)
+    assert orc.t2_matmul(x, packed, 1, 2, K).tolist() == [[-1048576, -1048576]]
+
+
 ALL_PINS = [pin_golden, pin_decoders, pin_pack_identity, pin_numpy_integer_matmul,
             pin_grouped_closed_form, pin_symmetric_equals_zero8, pin_int8_numpy, pin_slicing,
-            pin_dequant_closed_form]
+            pin_dequant_closed_form, pin_t2_numpy]

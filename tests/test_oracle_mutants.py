@@ -35,6 +35,11 @@ MUTANTS = {
     "int8-scale-index": ("wq_oracle_f32_to_f64(scale_bits[n]) * acc", "wq_oracle_f32_to_f64(scale_bits[0]) * acc"),
     "group-index": ("int g = k / group_size;\n        /* row k", "int g = (k / group_size) / 2;\n        /* row k"),
     "dequant-zero-sign": ("w[(size_t)k * N + n] = (q - z) * s;", "w[(size_t)k * N + n] = (q + z) * s;"),
+    "t2-plane-row-swap": ("(packed[(size_t)(k % R) * N + n] >> (2 * (k / R)))",
+                          "(packed[(size_t)(k / R) * N + n] >> (2 * (k % R)))"),
+    "t2-no-offset": ("& 3u) - 1;\n}", "& 3u);\n}"),
+    "t2-field-width": ("(packed[(size_t)(k % R) * N + n] >> (2 * (k / R))) & 3u)",
+                       "(packed[(size_t)(k % R) * N + n] >> (k / R)) & 3u)"),
     "dequant-scale-row": ("double s = decode16(scales[(size_t)g * N + n], s_is_bf16);\n            w[",
                           "double s = decode16(scales[(size_t)(k % (K / group_size)) * N + n], s_is_bf16);\n            w["),
 }
