@@ -224,6 +224,41 @@ WQ_API wq_status wq_matmul_noalloc(const void *x, wq_dtype x_dtype, const void *
                                    float *out, void *stream);
 
 /*
+ * Ternary int2 (Liger kernels, ops/experimental/mm_int8int2.py):
+ * weights in {-1, 0, 1} stored plus one as 2-bit fields of uint8, planar
+ * along K (pack_weights: with R = K / 4 byte rows, bits 2i, 2i + 1 of byte
+ * [k - i R][n] hold row k = i R + (k - i R)); int8 activations; the product
+ * accumulated in int32 (matmul_kernel):
+ *   y[m, n] = sum_k x[m, k] * (((q[k mod R][n] >> (2 (k div R))) & 3) - 1).
+ * A field value of 3 stands for weight 2 (unpack_weights subtracts 1 from
+ * every field).
+ *
+ * wq_t2_pack -- repack the planar bytes (K / 4, N) uint8 into the tiled
+ * 2-bit layout wq_t2_matmul reads (K * N / 4 bytes, wq_packed_bytes(K, N, 2)).
+ * Requirements: K % 128 == 0, K <= 65536, N % 16 == 0, N <= 262144; both
+ * pointers 16-byte aligned and not overlapping.
+ */
+WQ_API wq_status wq_t2_pack(const void *q_in, int K, int N, void *packed_out, void *stream);
+
+/*
+ * Bytes of scratch wq_t2_matmul needs: the activations converted to bf16
+ * (exact for int8), after any split-K partial sums of the few-token kernel
+ * (same conventions as wq_workspace_bytes: zero-filled once before first use,
+ * left reusable by every completed call, not shared by concurrent calls).
+ */
+WQ_API size_t wq_t2_workspace_bytes(int M, int N, int K);
+
+/*
+ * wq_t2_matmul -- y (M, N) int32 = x (M, K) int8 times the ternary weights
+ * (output of wq_t2_pack).  Every product and partial sum is an integer below
+ * 2^24 in magnitude (|x| <= 128, |w| <= 2, K <= 65536), so the tensor cores'
+ * fp32 accumulation is exact and y equals the int32 result bit for bit.
+ * x, packed_w, out and workspace 16-byte aligned; statuses as wq_matmul.
+ */
+WQ_API wq_status wq_t2_matmul(const int8_t *x, const void *packed_w, int M, int N, int K,
+                              int32_t *out, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * wq_matmul_path -- which kernel family wq_matmul runs for this problem:
  * 0 the few-token kernel (TMA ring, register dequant, mma.sync, split-K in
  * clusters), 1 the exact tensor-core kernel (tcgen05, q - zero exact, group

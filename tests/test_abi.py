@@ -163,3 +163,19 @@ def test_matmul_path_rules(L):
     assert P(64, 4096, 3, 128, BF16, BF16) == -1
     assert P(64, 4096, 4, 48, BF16, BF16) == -1
     assert P(64, 4096, 8, -1, BF16, BF16) == -1
+
+
+def test_t2_host_validation(L):
+    S = {n: i for i, n in enumerate(binding.STATUS)}
+    assert L.wq_t2_pack(None, 128, 16, FAKE, None) == S["WQ_ERR_NULL"]
+    assert L.wq_t2_pack(FAKE, 64, 16, FAKE, None) == S["WQ_ERR_SHAPE"]      # K not a multiple of 128
+    assert L.wq_t2_pack(FAKE, 128, 24, FAKE, None) == S["WQ_ERR_SHAPE"]     # N not a multiple of 16
+    assert L.wq_t2_pack(FAKE, 65536 + 128, 16, FAKE, None) == S["WQ_ERR_SHAPE"]  # sums could pass 2^24
+    assert L.wq_t2_pack(FAKE + 4, 128, 16, FAKE, None) == S["WQ_ERR_ALIGN"]
+    mm = L.wq_t2_matmul
+    assert mm(None, FAKE, 4, 16, 128, FAKE, FAKE, 1 << 20, None) == S["WQ_ERR_NULL"]
+    assert mm(FAKE, FAKE, 4, 16, 100, FAKE, FAKE, 1 << 20, None) == S["WQ_ERR_SHAPE"]
+    assert mm(FAKE, FAKE, -1, 16, 128, FAKE, FAKE, 1 << 20, None) == S["WQ_ERR_SHAPE"]
+    assert mm(FAKE + 8, FAKE, 4, 16, 128, FAKE, FAKE, 1 << 20, None) == S["WQ_ERR_ALIGN"]
+    assert mm(FAKE, FAKE, 0, 16, 128, FAKE, FAKE, 0, None) == S["WQ_OK"]
+    assert binding.wq_t2_workspace_bytes(4, 16, 100) == 0

@@ -22,7 +22,7 @@ STATUS = ["WQ_OK", "WQ_ERR_NULL", "WQ_ERR_SHAPE", "WQ_ERR_WBIT", "WQ_ERR_GROUP",
 
 EXPORTS = ("wq_status_string", "wq_chunk_k", "wq_packed_bytes", "wq_pack", "wq_unpack",
            "wq_workspace_bytes", "wq_matmul", "wq_matmul_ex", "wq_matmul_noalloc", "wq_matmul_path",
-           "wq_check_device")
+           "wq_t2_pack", "wq_t2_workspace_bytes", "wq_t2_matmul", "wq_check_device")
 
 PATHS = {0: "decode_kernel", 1: "midm_kernel", 2: "prefill_kernel"}
 
@@ -63,6 +63,12 @@ def lib() -> ctypes.CDLL:
         L.wq_matmul_ex.argtypes = [P, I, P, P, I, P, I, I, I, I, I, P, I, P, Z, P]
         L.wq_matmul_noalloc.restype = I
         L.wq_matmul_noalloc.argtypes = [P, I, P, P, I, P, I, I, I, I, I, P, P]
+        L.wq_t2_pack.restype = I
+        L.wq_t2_pack.argtypes = [P, I, I, P, P]
+        L.wq_t2_workspace_bytes.restype = Z
+        L.wq_t2_workspace_bytes.argtypes = [I, I, I]
+        L.wq_t2_matmul.restype = I
+        L.wq_t2_matmul.argtypes = [P, P, I, I, I, P, P, Z, P]
         L.wq_matmul_path.restype = I
         L.wq_matmul_path.argtypes = [I, I, I, I, I, I]
         L.wq_check_device.restype = I
@@ -186,6 +192,41 @@ def wq_matmul_noalloc(x: torch.Tensor, packed_w: torch.Tensor, scales: torch.Ten
                                  _DTYPE.get(scales.dtype, -1), _ptr(zeros), M, N, K, w_bit, group_size,
                                  _ptr(out), _stream(stream))
     _check(st, "wq_matmul_noalloc")
+    return out
+
+
+def wq_t2_pack(q_in: torch.Tensor, K: int, N: int, packed_out: torch.Tensor | None = None,
+               stream=None) -> torch.Tensor:
+    """Repack Liger planar ternary bytes (K/4, N) uint8 into the tiled 2-bit layout."""
+    if packed_out is None:
+        packed_out = torch.empty(max(K * N // 4, 16), dtype=torch.uint8, device=q_in.device)
+    _check(lib().wq_t2_pack(_ptr(q_in), K, N, _ptr(packed_out), _stream(stream)), "wq_t2_pack")
+    return packed_out
+
+
+def wq_t2_workspace_bytes(M: int, N: int, K: int) -> int:
+    return lib().wq_t2_workspace_bytes(M, N, K)
+
+
+_t2_workspaces: dict = {}
+
+
+def wq_t2_matmul(x: torch.Tensor, packed_w: torch.Tensor, M: int, N: int, K: int,
+                 out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                 stream=None) -> torch.Tensor:
+    """y (M, N) int32 = x (M, K) int8 @ ternary weights, through wq_t2_matmul."""
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.int32, device=x.device)
+    if workspace is None:
+        need = wq_t2_workspace_bytes(M, N, K)
+        dkey = torch.device(x.device).index
+        workspace = _t2_workspaces.get(dkey)
+        if need and (workspace is None or workspace.numel() < need):
+            workspace = _t2_workspaces[dkey] = torch.zeros(need, dtype=torch.uint8, device=x.device)
+    ws_bytes = 0 if workspace is None else workspace.numel()
+    st = lib().wq_t2_matmul(_ptr(x), _ptr(packed_w), M, N, K, _ptr(out), _ptr(workspace), ws_bytes,
+                            _stream(stream))
+    _check(st, "wq_t2_matmul")
     return out
 
 

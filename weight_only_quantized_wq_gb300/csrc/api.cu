@@ -124,6 +124,8 @@ wq_status prepare_call(const void *x, wq_dtype x_dtype, const void *packed_w, co
   a.group_size = group_size;
   a.x_bf16 = (x_dtype == WQ_BF16);
   a.s_bf16 = (s_dtype == WQ_BF16);
+  a.unit_scale = false;
+  a.sym_zero = w_bit == 8 ? 0 : 1 << (w_bit - 1);
   a.err = d->status;
   c->sms = d->sms;
   c->route = route_of(a);
@@ -148,12 +150,13 @@ wq_status run_call(const Call &c, void *workspace, void *stream) {
   MatmulArgs a = c.a;
   const int M = c.a.M, N = a.N, K = a.K;
   const bool zero = a.zeros != nullptr;
-  const DecodePlan full = plan_decode(M < 64 ? M : 64, N, K, a.w_bit, a.group_size, zero, c.sms);
+  const DecodePlan full = plan_decode(M < 64 ? M : 64, N, K, a.w_bit, a.group_size, zero, c.sms, a.unit_scale);
   for (int m0 = 0; m0 < M; m0 += 64) {
     a.M = (M - m0) < 64 ? (M - m0) : 64;
     a.x = static_cast<const uint16_t *>(c.a.x) + (size_t)m0 * K;
-    a.out = static_cast<char *>(c.a.out) + (size_t)m0 * N * (a.out_type == kOutF32 ? 4 : 2);
-    const DecodePlan p = (a.M == (M < 64 ? M : 64)) ? full : plan_decode(a.M, N, K, a.w_bit, a.group_size, zero, c.sms);
+    a.out = static_cast<char *>(c.a.out) + (size_t)m0 * N * (a.out_type == kOutF32 || a.out_type == kOutS32 ? 4 : 2);
+    const DecodePlan p =
+        (a.M == (M < 64 ? M : 64)) ? full : plan_decode(a.M, N, K, a.w_bit, a.group_size, zero, c.sms, a.unit_scale);
     if (launch_decode(a, p, workspace, s) != cudaSuccess) return WQ_ERR_CUDA;
   }
   return WQ_OK;
@@ -250,6 +253,93 @@ wq_status wq_matmul(const void *x, wq_dtype x_dtype, const void *packed_w, const
                     void *workspace, size_t workspace_bytes, void *stream) {
   return wq_matmul_ex(x, x_dtype, packed_w, scales, s_dtype, zeros, M, N, K, w_bit, group_size, out, WQ_F32,
                       workspace, workspace_bytes, stream);
+}
+
+// ------------------------------------------------------------------ ternary int2
+static wq_status check_t2(int K, int N) {
+  if (K <= 0 || N <= 0 || N % 16 != 0 || K % 128 != 0 || N > wq::kMaxN) return WQ_ERR_SHAPE;
+  if (K > 65536) return WQ_ERR_SHAPE;  // beyond, an fp32 partial sum could exceed 2^24
+  return WQ_OK;
+}
+
+static size_t t2_x_bytes(int M, int K) { return ((size_t)M * K * 2 + 255) / 256 * 256; }
+
+// Decode-kernel workspace of a ternary call (64-row slices, unit scale, zero 1).
+static size_t t2_decode_workspace(int M, int N, int K, int sms) {
+  size_t ws = wq::plan_decode(M < 64 ? M : 64, N, K, 2, K, false, sms, true).workspace;
+  if (M > 64 && M % 64 != 0) {
+    const size_t r = wq::plan_decode(M % 64, N, K, 2, K, false, sms, true).workspace;
+    ws = r > ws ? r : ws;
+  }
+  return ws;
+}
+
+wq_status wq_t2_pack(const void *q_in, int K, int N, void *packed_out, void *stream) {
+  if (!q_in || !packed_out) return WQ_ERR_NULL;
+  wq_status st = check_t2(K, N);
+  if (st != WQ_OK) return st;
+  if (!aligned(q_in, 16) || !aligned(packed_out, 16)) return WQ_ERR_ALIGN;
+  DeviceInfo *d = nullptr;
+  if ((st = device_info(&d)) != WQ_OK) return st;
+  return wq::launch_t2_pack(q_in, packed_out, K, N, static_cast<cudaStream_t>(stream)) == cudaSuccess ? WQ_OK
+                                                                                                       : WQ_ERR_CUDA;
+}
+
+// Offset of the converted activations in a ternary call's workspace: after
+// the few-token kernel's counters and partial sums, and never over the
+// counters even when this call needs none (another call sharing the
+// workspace may, and relies on them staying zero).
+static size_t t2_x_offset(size_t dec) {
+  const size_t lo = dec > wq::decode_counter_bytes() ? dec : wq::decode_counter_bytes();
+  return (lo + 255) / 256 * 256;
+}
+
+size_t wq_t2_workspace_bytes(int M, int N, int K) {
+  if (M <= 0 || check_t2(K, N) != WQ_OK) return 0;
+  DeviceInfo *d = nullptr;
+  if (device_info(&d) != WQ_OK) return 0;
+  return t2_x_offset(t2_decode_workspace(M, N, K, d->sms)) + t2_x_bytes(M, K);
+}
+
+wq_status wq_t2_matmul(const int8_t *x, const void *packed_w, int M, int N, int K, int32_t *out, void *workspace,
+                       size_t workspace_bytes, void *stream) {
+  if (!x || !packed_w || !out) return WQ_ERR_NULL;
+  if (M < 0 || N < 0 || K <= 0) return WQ_ERR_SHAPE;
+  if (M == 0 || N == 0) return WQ_OK;
+  wq_status st = check_t2(K, N);
+  if (st != WQ_OK) return st;
+  if (!aligned(x, 16) || !aligned(packed_w, 16) || !aligned(out, 16)) return WQ_ERR_ALIGN;
+  DeviceInfo *d = nullptr;
+  if ((st = device_info(&d)) != WQ_OK) return st;
+  const size_t dec = t2_decode_workspace(M, N, K, d->sms);
+  const size_t xoff = t2_x_offset(dec);
+  if (!workspace || workspace_bytes < xoff + t2_x_bytes(M, K)) return WQ_ERR_WORKSPACE;
+  if (!aligned(workspace, 16)) return WQ_ERR_ALIGN;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  void *xb = static_cast<char *>(workspace) + xoff;
+  if (wq::launch_int8_to_bf16(x, xb, (size_t)M * K, s) != cudaSuccess) return WQ_ERR_CUDA;
+  wq::Call c;
+  wq::MatmulArgs &a = c.a;
+  a.x = xb;
+  a.packed = packed_w;
+  a.scales = nullptr;
+  a.zeros = nullptr;
+  a.out = out;
+  a.out_type = wq::kOutS32;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.w_bit = 2;
+  a.group_size = K;
+  a.x_bf16 = true;
+  a.s_bf16 = true;
+  a.unit_scale = true;
+  a.sym_zero = 1;  // codes are the weights plus one
+  a.err = d->status;
+  c.sms = d->sms;
+  c.route = wq::Route::kDecode;
+  c.need = dec;
+  return wq::run_call(c, dec > 0 ? workspace : nullptr, stream);
 }
 
 int wq_matmul_path(int M, int K, int w_bit, int group_size, wq_dtype x_dtype, wq_dtype s_dtype) {

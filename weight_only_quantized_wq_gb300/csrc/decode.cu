@@ -77,7 +77,8 @@ static long capacity(int w_bit, int fold, int mt, int tn, bool zero, int smem, i
   return c;
 }
 
-static DecodePlan plan_decode_search(int M, int N, int K, int w_bit, int group_size, bool zero, int sms) {
+static DecodePlan plan_decode_search(int M, int N, int K, int w_bit, int group_size, bool zero, int sms,
+                                     bool unit_scale) {
   DecodePlan best{};
   const int rows = M < 64 ? M : 64;
   const int mt = rows <= 8 ? 1 : rows <= 16 ? 2 : rows <= 32 ? 4 : 8;
@@ -101,6 +102,7 @@ static DecodePlan plan_decode_search(int M, int N, int K, int w_bit, int group_s
     if (s != sreal) continue;
     int srows = 0, zwrows = 0;
     if (grouped) rows_for(K, kc, gs, cps, V, &srows, &zwrows);
+    if (unit_scale) srows = 0;  // no scale rows are staged
     if (!zero) zwrows = 0;
     const int zrows = zero ? srows : 0;  // one (MAGIC + zero) row per group
     if (srows > 256 || zwrows > 256) continue;  // one TMA box each
@@ -154,19 +156,19 @@ static DecodePlan plan_decode_search(int M, int N, int K, int w_bit, int group_s
 
 // The plan of a shape, searched once per device and shape (a call then costs
 // one lookup instead of a search over every split count).
-DecodePlan plan_decode(int M, int N, int K, int w_bit, int group_size, bool zero, int sms) {
+DecodePlan plan_decode(int M, int N, int K, int w_bit, int group_size, bool zero, int sms, bool unit_scale) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) dev = -1;
-  using Key = std::tuple<int, int, int, int, int, int, bool, int>;
+  using Key = std::tuple<int, int, int, int, int, int, bool, int, bool>;
   static std::map<Key, DecodePlan> cache;
   static std::mutex mu;
-  const Key key{dev, M, N, K, w_bit, group_size, zero, sms};
+  const Key key{dev, M, N, K, w_bit, group_size, zero, sms, unit_scale};
   {
     std::lock_guard<std::mutex> lock(mu);
     auto it = cache.find(key);
     if (it != cache.end()) return it->second;
   }
-  const DecodePlan p = plan_decode_search(M, N, K, w_bit, group_size, zero, sms);
+  const DecodePlan p = plan_decode_search(M, N, K, w_bit, group_size, zero, sms, unit_scale);
   std::lock_guard<std::mutex> lock(mu);
   if (cache.size() > 4096) cache.clear();  // bounded: a process with many shapes searches again
   cache.emplace(key, p);
@@ -193,6 +195,8 @@ cudaError_t launch_decode(const MatmulArgs &a, const DecodePlan &p, void *worksp
   dp.zrows = p.zrows;
   dp.zwrows = p.zwrows;
   dp.s_bf16 = a.s_bf16;
+  dp.unit_scale = a.unit_scale;
+  dp.sym_zero = a.sym_zero;
   dp.cluster = p.cluster;
   if (p.splits > 1 && !p.cluster) {
     dp.counters = static_cast<int *>(workspace);
@@ -205,7 +209,7 @@ cudaError_t launch_decode(const MatmulArgs &a, const DecodePlan &p, void *worksp
   const uint32_t cols = (uint32_t)(kDecodeWarps * p.tn * 16);
   if (a.w_bit != 8) {
     const int G = a.K / a.group_size, V = 32 / a.w_bit;
-    if (!encode_2d(&dp.tm_s, a.scales, 2, (uint64_t)a.N, (uint64_t)G, cols, (uint32_t)p.srows))
+    if (!a.unit_scale && !encode_2d(&dp.tm_s, a.scales, 2, (uint64_t)a.N, (uint64_t)G, cols, (uint32_t)p.srows))
       return cudaErrorInvalidValue;
     if (a.zeros && !encode_2d(&dp.tm_z, a.zeros, 4, (uint64_t)a.N, (uint64_t)((G + V - 1) / V), cols, (uint32_t)p.zwrows))
       return cudaErrorInvalidValue;

@@ -106,6 +106,8 @@ struct DecodeParams {
   int *counters;
   uint32_t *err;
   int M, N, K, gs, nt_total, kch, splits, cps, srows, zrows, zwrows;
+  int sym_zero;     // zero of every group without zero words
+  bool unit_scale;  // every group scale is 1 (no scale rows)
   bool s_bf16;
   bool cluster;  // the splits of a column block form a cluster (reduction in shared memory)
 };
@@ -169,7 +171,7 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_min_blocks(MT, TN))
     if (GROUPED && lane == 0) {  // this CTA's scale rows (and zero-word rows) ahead of the ring
       const uint32_t mb = smem_addr(meta);
       mbar_arrive_expect_tx(mb, (uint32_t)(L.srows * CC * 2 + L.zwrows * CC * 4));
-      tma_load_2d(smem_addr(smem + L.s_off()), &p.tm_s, n0, g0, mb);
+      if (!p.unit_scale) tma_load_2d(smem_addr(smem + L.s_off()), &p.tm_s, n0, g0, mb);
       if (ZERO) tma_load_2d(smem_addr(smem + L.zw_off()), &p.tm_z, n0, g0 / V, mb);
     }
     if (lane == 0) {
@@ -258,7 +260,7 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_min_blocks(MT, TN))
         if constexpr (ZERO)
           zz[ti][rr] = z_sm[(gi - g0) * CC + (wt0 + ti) * 16 + g + 8 * rr];
         else
-          zz[ti][rr] = ((Magic<BF16>::kPair & 0xFFFFu) + (1u << (W - 1))) * 0x00010001u;
+          zz[ti][rr] = ((Magic<BF16>::kPair & 0xFFFFu) + (uint32_t)p.sym_zero) * 0x00010001u;
         if constexpr (kOddFma) zz16[ti][rr] = sub_pair<false>(kF16NineSixty, zz[ti][rr]);
       }
   };
@@ -268,7 +270,8 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_min_blocks(MT, TN))
     for (int ti = 0; ti < TN; ++ti)
 #pragma unroll
       for (int rr = 0; rr < 2; ++rr) {
-        const float s = half_bits_to_float(s_sm[(gi - g0) * CC + (wt0 + ti) * 16 + g + 8 * rr], p.s_bf16);
+        const float s =
+            p.unit_scale ? 1.f : half_bits_to_float(s_sm[(gi - g0) * CC + (wt0 + ti) * 16 + g + 8 * rr], p.s_bf16);
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt)
 #pragma unroll

@@ -307,6 +307,9 @@ __device__ __forceinline__ uint32_t int8_pair(uint32_t w, int hi_half) {
 __device__ __forceinline__ void store_out4(void *out, size_t idx, float4 v, int ot) {
   if (ot == kOutF32) {
     *reinterpret_cast<float4 *>(static_cast<float *>(out) + idx) = v;
+  } else if (ot == kOutS32) {
+    *reinterpret_cast<int4 *>(static_cast<int *>(out) + idx) =
+        make_int4(__float2int_rn(v.x), __float2int_rn(v.y), __float2int_rn(v.z), __float2int_rn(v.w));
   } else if (ot == kOutF16) {
     __half2 a = __floats2half2_rn(v.x, v.y), b = __floats2half2_rn(v.z, v.w);
     *reinterpret_cast<uint2 *>(static_cast<__half *>(out) + idx) =
@@ -321,6 +324,8 @@ __device__ __forceinline__ void store_out4(void *out, size_t idx, float4 v, int 
 __device__ __forceinline__ void store_out1(void *out, size_t idx, float v, int ot) {
   if (ot == kOutF32)
     static_cast<float *>(out)[idx] = v;
+  else if (ot == kOutS32)
+    static_cast<int *>(out)[idx] = __float2int_rn(v);
   else if (ot == kOutF16)
     static_cast<__half *>(out)[idx] = __float2half_rn(v);
   else

@@ -17,10 +17,14 @@ bool encode_2d(CUtensorMap *m, const void *base, int elem_bytes, uint64_t cols, 
 
 cudaError_t launch_pack(const void *qin, void *out, int K, int N, int w_bit, cudaStream_t s);
 cudaError_t launch_unpack(const void *packed, uint8_t *codes, int K, int N, int w_bit, cudaStream_t s);
+// Liger planar ternary bytes (K/4, N) -> the 2-bit tiled layout (codes = weight + 1).
+cudaError_t launch_t2_pack(const void *qin, void *out, int K, int N, cudaStream_t s);
+// n int8 values (n % 4 == 0) -> bf16, exactly.
+cudaError_t launch_int8_to_bf16(const void *x, void *y, size_t n, cudaStream_t s);
 
 // Output element types of the matmul epilogues: the fp32 result is stored as
 // is or rounded once (to nearest even) to fp16 or bf16.
-enum OutType : int { kOutF32 = 0, kOutF16 = 1, kOutBF16 = 2 };
+enum OutType : int { kOutF32 = 0, kOutF16 = 1, kOutBF16 = 2, kOutS32 = 3 };  // S32: integer-valued results
 
 // Problem handed to the matmul kernels after host validation.
 struct MatmulArgs {
@@ -32,6 +36,8 @@ struct MatmulArgs {
   int out_type;           // OutType: fp32, fp16 or bf16
   int M, N, K, w_bit, group_size;
   bool x_bf16, s_bf16;
+  bool unit_scale;        // no scales: every group scale is 1 (scales unused)
+  int sym_zero;           // zero of every group when zeros == nullptr
   uint32_t *err;          // device status word
 };
 
@@ -60,7 +66,7 @@ constexpr int kMaxColumnBlocks = 4096;
 constexpr int kMaxN = 16 * 4 * kMaxColumnBlocks;  // 262144 output channels
 size_t decode_counter_bytes();
 
-DecodePlan plan_decode(int M, int N, int K, int w_bit, int group_size, bool zero, int sms);
+DecodePlan plan_decode(int M, int N, int K, int w_bit, int group_size, bool zero, int sms, bool unit_scale = false);
 cudaError_t launch_decode(const MatmulArgs &a, const DecodePlan &p, void *workspace, cudaStream_t s);
 
 // Tensor-core path for many tokens (int4 codes, group size a multiple of 64,

@@ -64,6 +64,43 @@ __global__ void unpack_kernel(const uint32_t *__restrict__ packed, uint8_t *__re
   }
 }
 
+// Liger planar ternary bytes (K/4, N) -> the tiled 2-bit layout, one thread
+// per output word: the code of (k, n) is field k div R of byte [k mod R][n],
+// R = K / 4 (ops/experimental/mm_int8int2.py, pack_weights).  The codes are
+// the stored values (weight + 1), so the matmul subtracts 1 as its zero.
+__global__ void t2_pack_kernel(const uint8_t *__restrict__ qin, uint32_t *__restrict__ out, int K, int N) {
+  using G = Geo<2>;
+  const int NT = N / 16, R = K / 4;
+  const size_t total = (size_t)K / G::V * N;
+  for (size_t o = (size_t)blockIdx.x * blockDim.x + threadIdx.x; o < total; o += (size_t)gridDim.x * blockDim.x) {
+    const int wi = (int)(o & 3), lane = (int)((o >> 2) & 31);
+    const size_t tile = o >> 7;
+    const int nt = (int)(tile % NT);
+    const int kc = (int)(tile / NT);
+    uint32_t word = 0;
+#pragma unroll
+    for (int f = 0; f < G::V; ++f) {
+      int kk, nn;
+      field_coords<2>(lane, wi, f, kk, nn);
+      const int k = kc * G::KC + kk, n = nt * 16 + nn;
+      const uint32_t code = (qin[(size_t)(k % R) * N + n] >> (2 * (k / R))) & 3u;
+      word |= code << (f * 2);
+    }
+    out[o] = word;
+  }
+}
+
+// int8 activations -> bf16 (exact: |x| <= 128 needs 8 significant bits),
+// four per thread.
+__global__ void int8_to_bf16_kernel(const char4 *__restrict__ x, uint2 *__restrict__ y, size_t n4) {
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x) {
+    const char4 v = x[i];
+    const uint32_t a = (uint32_t)__float_as_uint((float)v.x) >> 16 | ((uint32_t)__float_as_uint((float)v.y) & 0xFFFF0000u);
+    const uint32_t b = (uint32_t)__float_as_uint((float)v.z) >> 16 | ((uint32_t)__float_as_uint((float)v.w) & 0xFFFF0000u);
+    y[i] = make_uint2(a, b);
+  }
+}
+
 static int grid_for(size_t n) {
   size_t b = (n + 255) / 256;
   return (int)(b > 65535 * 4 ? 65535 * 4 : (b ? b : 1));
@@ -78,6 +115,18 @@ cudaError_t launch_pack(const void *qin, void *out, int K, int N, int w_bit, cud
     case 8: pack_kernel<8><<<grid, 256, 0, s>>>(qin, (uint32_t *)out, K, N); break;
     default: return cudaErrorInvalidValue;
   }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_t2_pack(const void *qin, void *out, int K, int N, cudaStream_t s) {
+  const size_t words = (size_t)K * N / 16;
+  t2_pack_kernel<<<grid_for(words), 256, 0, s>>>(static_cast<const uint8_t *>(qin), (uint32_t *)out, K, N);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_int8_to_bf16(const void *x, void *y, size_t n, cudaStream_t s) {
+  const size_t n4 = n / 4;
+  int8_to_bf16_kernel<<<grid_for(n4), 256, 0, s>>>(static_cast<const char4 *>(x), static_cast<uint2 *>(y), n4);
   return cudaGetLastError();
 }
 

@@ -99,6 +99,52 @@ def int8(name, M, K, N, x_dtype, s_range, seed=0, int_exact=False) -> Problem:
     return Problem(name, M, K, N, 8, K, x_dtype, F32, x, q, s, None)
 
 
+@dataclasses.dataclass
+class TernaryProblem:
+    """Liger planar ternary problem: x (M, K) int8, packed (K/4, N) uint8."""
+    name: str
+    M: int
+    K: int
+    N: int
+    x: torch.Tensor
+    packed: torch.Tensor
+
+    @property
+    def flops(self) -> int:
+        return 2 * self.M * self.K * self.N
+
+    def weight_bytes(self) -> int:
+        return self.packed.numel()
+
+    def total_bytes(self) -> int:
+        """Algorithmic bytes: packed weights + int8 x + int32 y, each once."""
+        return self.packed.numel() + self.x.numel() + self.M * self.N * 4
+
+
+# bytes whose four 2-bit fields are all below 3 (weights -1, 0, 1 stored plus one)
+_TERNARY_BYTES = torch.tensor([b for b in range(256) if all((b >> (2 * i)) & 3 != 3 for i in range(4))],
+                              dtype=torch.uint8)
+
+
+def ternary(name, M, K, N, seed=0, all_fields=False) -> TernaryProblem:
+    """x uniform int8 in [-128, 127]; each packed byte uniform over the bytes
+    whose fields are all 0..2 (ternary weights), or over all 256 bytes
+    (all_fields: field 3, weight 2, included)."""
+    gen = torch.Generator("cpu").manual_seed(seed)
+    x = torch.randint(-128, 128, (M, K), generator=gen, dtype=torch.int64).to(torch.int8)
+    if all_fields:
+        packed = torch.randint(0, 256, (K // 4, N), generator=gen, dtype=torch.int64).to(torch.uint8)
+    else:
+        idx = torch.randint(0, len(_TERNARY_BYTES), (K // 4, N), generator=gen, dtype=torch.int64)
+        packed = _TERNARY_BYTES[idx]
+    return TernaryProblem(name, M, K, N, x, packed)
+
+
+def ternary_decode(seed=0):
+    """Ternary int2 (BitNet-style) decode: M=16, K=8192, N=8192."""
+    return ternary("ternary-int2 M16 K8192 N8192", 16, 8192, 8192, seed=seed)
+
+
 # The five workloads, with the sizes and distributions of the statement of the problem.
 def int4_asym_tiny(seed=0):
     """int4 asymmetric, group 128: M=1, K=512, N=512, fp16 x and scales."""
