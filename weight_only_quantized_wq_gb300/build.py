@@ -36,6 +36,10 @@ def nvcc() -> str:
 DECODE_VARIANTS = [(2, 0), (2, 2), (2, 4), (2, -1), (4, 0), (4, 2), (4, -1), (8, 0)]
 
 
+FLOOR_SRC = os.path.join(PKG, "bench_csrc", "floor.cu")
+FLOOR_LIB = os.path.join(PKG, "libwqfloor.so")
+
+
 def _sources():
     return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
 
@@ -64,6 +68,18 @@ def up_to_date() -> bool:
         return False
     t = os.path.getmtime(LIB)
     return all(os.path.getmtime(d) <= t for d in _deps())
+
+
+def build_floor(force: bool = False) -> str:
+    """The benchmark's read-only streaming kernel, in a library of its own."""
+    if not force and os.path.exists(FLOOR_LIB) and os.path.getmtime(FLOOR_LIB) >= os.path.getmtime(FLOOR_SRC):
+        return FLOOR_LIB
+    tmp = FLOOR_LIB + ".%d.tmp" % os.getpid()
+    r = subprocess.run([nvcc(), *ARCH, *FLAGS, "-shared", "-o", tmp, FLOOR_SRC], capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError("nvcc failed on %s:\n%s%s" % (FLOOR_SRC, r.stdout, r.stderr))
+    os.replace(tmp, FLOOR_LIB)
+    return FLOOR_LIB
 
 
 def build(force: bool = False, verbose: bool = False, extra: list[str] | None = None) -> str:
