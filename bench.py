@@ -400,11 +400,15 @@ def roofline_entry(b, sec_per_call, pk, src, floor=None):
 def sweep(torch, wq, syn, l2, pk, src, sms):
     out = []
     c5 = syn.int4_asym_sweep(4096)
-    runs = [(syn.int4_asym_tiny(), "f32"), (syn.int8_per_channel(), "f32"), (syn.int4_sym_decode(), "f32"),
-            (syn.int2_asym(), "f32")]
-    runs += [(c5.rows(m), "f32") for m in syn.C5_MS]
-    runs += [(c5.rows(16), "bf16"), (c5.rows(1024), "bf16"), (syn.ternary_decode(), "s32")]
-    for p, odt in runs:
+    runs = [(syn.int4_asym_tiny(), "f32", "int4_asym_tiny|M=1"), (syn.int8_per_channel(), "f32", "int8_per_channel|M=16"),
+            (syn.int4_sym_decode(), "f32", "int4_sym_decode|M=1"), (syn.int2_asym(), "f32", "int2_asym|M=8")]
+    runs += [(c5.rows(m), "f32", "int4_asym_sweep|M=%d" % m) for m in syn.C5_MS]
+    runs += [(c5.rows(16), "bf16", "int4_asym_sweep|M=16|out=bf16"),
+             (c5.rows(1024), "bf16", "int4_asym_sweep|M=1024|out=bf16"),
+             (syn.ternary_decode(), "s32", "ternary_decode|M=16"),
+             (syn.int4_asym_short_k(128), "f32", "int4_asym_short_k|M=128"),
+             (syn.int4_asym_short_k(1024), "f32", "int4_asym_short_k|M=1024")]
+    for p, odt, key in runs:
         b = Bench(p, torch, wq, l2, out_dtype="f32" if odt == "s32" else odt)
         n = 50 if p.M <= 256 else 10
         sec = time_graphs(b, n, 5, torch) / n
@@ -414,6 +418,7 @@ def sweep(torch, wq, syn, l2, pk, src, sms):
              "TFLOPs": round(p.flops / sec / 1e12, 2)}
         fl = floor_us(b.total_bytes(), l2, torch, sms) if p.M <= 64 else None
         e["roofline"] = roofline_entry(b, sec, pk, src, fl)
+        e["roofline"]["traffic"] = traffic_for(key)
         out.append(e)
         del b
         torch.cuda.empty_cache()
@@ -506,10 +511,8 @@ def job_gbps(world, weight_bytes, steps, sec):
 
 def get_problem(args):
     from weight_only_quantized_wq_gb300 import synthetic as syn
-    if args.workload == "ternary_decode":
-        return syn.ternary_decode()
     f = syn.WORKLOADS[args.workload]
-    return f(args.m) if args.workload == "int4_asym_sweep" else f()
+    return f(args.m) if args.workload in ("int4_asym_sweep", "int4_asym_short_k") else f()
 
 
 def config_of(p, extra=None, out="fp32"):
@@ -585,8 +588,8 @@ def main():
     if not args.kernel_only and rank == 0 and p.M <= 64:
         fl = floor_us(b.total_bytes(), l2, torch, sms)
     roof = roofline_entry(b, per_step, pk, pk_src, fl)
-    key = "%s|M=%d" % (args.workload, p.M)
-    roof["traffic"] = traffic_for(key) if args.out_dtype == "f32" else None
+    key = "%s|M=%d" % (args.workload, p.M) + ("" if args.out_dtype == "f32" else "|out=" + args.out_dtype)
+    roof["traffic"] = traffic_for(key)
     roof["kernel"] = b.kernel_name()
     roof["launch_us"] = round(per_step / lpc * 1e6, 3)
 

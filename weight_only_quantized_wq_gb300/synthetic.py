@@ -177,10 +177,20 @@ def int4_asym_sweep(M=4096, seed=0):
     return p.rows(M)
 
 
+def int4_asym_short_k(M=128, seed=0):
+    """int4 asymmetric, group 128, K=2048, N=28672, bf16: a shorter K than the
+    sweep, where the many-token kernel's rounding of w to bf16 would not hold
+    the accepted error, so more than 64 tokens run on the exact path."""
+    return grouped("int4-asym-g128 K2048 N28672 M%d" % M, M, 2048, 28672, 4, 128, BF16, BF16, (0.002, 0.02),
+                   seed=seed)
+
+
 WORKLOADS = {
     "int4_asym_tiny": int4_asym_tiny,
     "int8_per_channel": int8_per_channel,
     "int4_sym_decode": int4_sym_decode,
     "int2_asym": int2_asym,
     "int4_asym_sweep": int4_asym_sweep,
+    "int4_asym_short_k": int4_asym_short_k,
+    "ternary_decode": ternary_decode,
 }
