@@ -34,6 +34,25 @@ def test_library_exports_every_declared_symbol(L):
     for name in declared():
         assert hasattr(L, name), name
         assert isinstance(getattr(L, name), ctypes._CFuncPtr)
+    src = open(os.path.join(ROOT, "include", "wq_testing.h")).read()
+    testing = re.findall(r"WQ_API[^;(]*?\b(wq_\w+)\s*\(", src)
+    assert set(testing) == set(binding.TESTING_EXPORTS)
+    for name in testing:
+        assert hasattr(L, name), name
+
+
+def test_testing_hook_validates_on_the_host(L):
+    S = {n: i for i, n in enumerate(binding.STATUS)}
+    f = L.wq_testing_decode_timeout
+    args = [FAKE, 1, FAKE, FAKE, 1, None, 4, 64, 128, 4, 64, FAKE, None, 0]
+    assert f(*args, 100, 1, None) == S["WQ_ERR_SHAPE"]            # limit too short
+    assert f(*args, 10 ** 10, 1, None) == S["WQ_ERR_SHAPE"]       # limit too long
+    assert f(*args, 100000, -1, None) == S["WQ_ERR_SHAPE"]        # no stage withheld
+    args[6] = 65
+    assert f(*args, 100000, 1, None) == S["WQ_ERR_SHAPE"]         # not the few-token kernel
+    args[6] = 4
+    args[0] = FAKE + 2
+    assert f(*args, 100000, 1, None) == S["WQ_ERR_ALIGN"]
 
 
 def test_status_strings(L):

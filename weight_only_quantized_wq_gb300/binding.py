@@ -26,6 +26,9 @@ EXPORTS = ("wq_status_string", "wq_chunk_k", "wq_packed_bytes", "wq_pack", "wq_u
 
 PATHS = {0: "decode_kernel", 1: "midm_kernel", 2: "prefill_kernel"}
 
+# the failure-path test hook of include/wq_testing.h
+TESTING_EXPORTS = ("wq_testing_decode_timeout",)
+
 
 class WQError(RuntimeError):
     def __init__(self, status: int, what: str):
@@ -71,6 +74,8 @@ def lib() -> ctypes.CDLL:
         L.wq_t2_matmul.argtypes = [P, P, I, I, I, P, P, Z, P]
         L.wq_matmul_path.restype = I
         L.wq_matmul_path.argtypes = [I, I, I, I, I, I]
+        L.wq_testing_decode_timeout.restype = I
+        L.wq_testing_decode_timeout.argtypes = [P, I, P, P, I, P, I, I, I, I, I, P, P, Z, ctypes.c_longlong, I, P]
         L.wq_check_device.restype = I
         L.wq_check_device.argtypes = [P]
         _lib = L
@@ -236,6 +241,25 @@ def wq_matmul_path(M: int, K: int, w_bit: int, group_size: int, x_dtype, s_dtype
     xd = _DTYPE.get(x_dtype, x_dtype)
     sd = _DTYPE.get(s_dtype, s_dtype)
     return lib().wq_matmul_path(M, K, w_bit, group_size, int(xd), int(sd))
+
+
+def wq_testing_decode_timeout(x: torch.Tensor, packed_w: torch.Tensor, scales: torch.Tensor,
+                              zeros: torch.Tensor | None, M: int, N: int, K: int, w_bit: int, group_size: int,
+                              wait_limit_cycles: int, withhold_stage: int, out: torch.Tensor | None = None,
+                              workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """The few-token kernel with a short barrier-wait limit and one withheld ring
+    stage (include/wq_testing.h): the failure path, without any fault."""
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    if workspace is None:
+        workspace = workspace_for(M, N, K, w_bit, group_size, x.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib().wq_testing_decode_timeout(_ptr(x), _DTYPE.get(x.dtype, -1), _ptr(packed_w), _ptr(scales),
+                                         _DTYPE.get(scales.dtype, -1), _ptr(zeros), M, N, K, w_bit, group_size,
+                                         _ptr(out), _ptr(workspace), ws_bytes, int(wait_limit_cycles),
+                                         int(withhold_stage), _stream(stream))
+    _check(st, "wq_testing_decode_timeout")
+    return out
 
 
 def wq_check_device(stream=None) -> None:

@@ -59,8 +59,8 @@ def _units():
 
 
 def _deps():
-    return _sources() + glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(CSRC, "*.h")) + [
-        os.path.join(INCLUDE, "wq.h")]
+    return _sources() + glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(CSRC, "*.h")) + glob.glob(
+        os.path.join(INCLUDE, "*.h"))
 
 
 def up_to_date() -> bool:

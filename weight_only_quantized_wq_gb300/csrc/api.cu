@@ -126,6 +126,8 @@ wq_status prepare_call(const void *x, wq_dtype x_dtype, const void *packed_w, co
   a.s_bf16 = (s_dtype == WQ_BF16);
   a.unit_scale = false;
   a.sym_zero = w_bit == 8 ? 0 : 1 << (w_bit - 1);
+  a.wait_limit = 0;  // the default limit
+  a.withhold = -1;
   a.err = d->status;
   c->sms = d->sms;
   c->route = route_of(a);
@@ -335,6 +337,8 @@ wq_status wq_t2_matmul(const int8_t *x, const void *packed_w, int M, int N, int 
   a.s_bf16 = true;
   a.unit_scale = true;
   a.sym_zero = 1;  // codes are the weights plus one
+  a.wait_limit = 0;
+  a.withhold = -1;
   a.err = d->status;
   c.sms = d->sms;
   c.route = wq::Route::kDecode;

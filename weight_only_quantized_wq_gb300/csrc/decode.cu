@@ -196,6 +196,8 @@ cudaError_t launch_decode(const MatmulArgs &a, const DecodePlan &p, void *worksp
   dp.zwrows = p.zwrows;
   dp.s_bf16 = a.s_bf16;
   dp.unit_scale = a.unit_scale;
+  dp.wait_limit = a.wait_limit > 0 ? a.wait_limit : kWaitLimitCycles;
+  dp.withhold = a.withhold;
   dp.sym_zero = a.sym_zero;
   dp.cluster = p.cluster;
   if (p.splits > 1 && !p.cluster) {

@@ -106,6 +106,8 @@ struct DecodeParams {
   int *counters;
   uint32_t *err;
   int M, N, K, gs, nt_total, kch, splits, cps, srows, zrows, zwrows;
+  long long wait_limit;  // SM cycles after which a barrier wait gives up
+  int withhold;          // test hook: ring stage the producer never arms or fills (-1: none)
   int sym_zero;     // zero of every group without zero words
   bool unit_scale;  // every group scale is 1 (no scale rows)
   bool s_bf16;
@@ -179,7 +181,15 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_min_blocks(MT, TN))
       uint32_t ph = 0;  // phase parity of the ring's current lap
       const int nst = (nch + kSlotsPerStage - 1) / kSlotsPerStage;
       for (int i = 0; i < nst; ++i) {
-        if (i >= STAGES && !mbar_wait(smem_addr(&empty[st]), ph ^ 1u, p.err, &s_abort)) break;
+        if (i >= STAGES && !mbar_wait(smem_addr(&empty[st]), ph ^ 1u, p.err, &s_abort, p.wait_limit)) break;
+        if (i == p.withhold) {  // test hook: the consumers' wait for this stage must run out
+          issued = i + 1;
+          if (++st == STAGES) {
+            st = 0;
+            ph ^= 1u;
+          }
+          continue;
+        }
         const uint32_t fb = smem_addr(&full[st]);
         const uint32_t base = smem_addr(ring + st * SB);
         const int ns = min(kSlotsPerStage, nch - i * kSlotsPerStage);
@@ -197,8 +207,8 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_min_blocks(MT, TN))
       }
       // No copy may still be writing this CTA's shared memory when it exits.
       for (int i = max(0, issued - STAGES); i < issued; ++i)
-        mbar_wait(smem_addr(&full[i % STAGES]), (i / STAGES) & 1, p.err, nullptr);
-      if (GROUPED) mbar_wait(smem_addr(meta), 0, p.err, nullptr);
+        if (i != p.withhold) mbar_wait(smem_addr(&full[i % STAGES]), (i / STAGES) & 1, p.err, nullptr, p.wait_limit);
+      if (GROUPED) mbar_wait(smem_addr(meta), 0, p.err, nullptr, p.wait_limit);
     }
     __syncwarp();
     if (p.cluster) {  // the consumers' two cluster barriers
@@ -217,7 +227,7 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_min_blocks(MT, TN))
   // and column, built once per CTA.
   const int g0 = GROUPED ? kbeg / p.gs : 0;
   if constexpr (GROUPED) {
-    const bool ok = mbar_wait(smem_addr(meta), 0, p.err, &s_abort);
+    const bool ok = mbar_wait(smem_addr(meta), 0, p.err, &s_abort, p.wait_limit);
     if (ZERO && ok) {
       const int ng = (kend - 1) / p.gs - g0 + 1;
       const int wr0 = g0 / V;
@@ -294,7 +304,7 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_min_blocks(MT, TN))
   int st = 0, st1 = 1 % STAGES;  // this stage and the next (ring positions)
   uint32_t ph = 0, ph1 = STAGES == 1 ? 1u : 0u;  // their phase parities
   for (int i = 0; i < nst; ++i) {
-    if (!next_ready && !mbar_wait(smem_addr(&full[st]), ph, p.err, &s_abort)) break;
+    if (!next_ready && !mbar_wait(smem_addr(&full[st]), ph, p.err, &s_abort, p.wait_limit)) break;
     if (i + 1 < nst) next_ready = mbar_test_wait(smem_addr(&full[st1]), ph1);
 #pragma unroll
     for (int sl = 0; sl < kSlotsPerStage; ++sl) {

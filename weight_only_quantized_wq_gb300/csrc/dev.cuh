@@ -76,18 +76,20 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Wait for the phase of `bar` with the given parity to complete.  Gives up
-// after kWaitLimitCycles, records kDevErrTimeout in *err, raises the CTA's abort
-// flag and returns false.  When `abort` is given, a raised flag (another
-// thread of the CTA gave up) also ends the wait at once; waits that must see
-// their copies land before the CTA exits pass nullptr.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t *err, volatile int *abort) {
+// after `limit` SM cycles (kWaitLimitCycles unless a caller lowers it),
+// records kDevErrTimeout in *err, raises the CTA's abort flag and returns
+// false.  When `abort` is given, a raised flag (another thread of the CTA gave
+// up) also ends the wait at once; waits that must see their copies land
+// before the CTA exits pass nullptr.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t *err, volatile int *abort,
+                                          long long limit = kWaitLimitCycles) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 255u) == 0u) {
       if (abort && *abort) return false;
-      if (clock64() - t0 > kWaitLimitCycles) {
+      if (clock64() - t0 > limit) {
         atomicOr(err, kDevErrTimeout);
         if (abort) *abort = 1;
         return false;

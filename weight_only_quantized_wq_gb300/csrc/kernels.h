@@ -38,6 +38,8 @@ struct MatmulArgs {
   bool x_bf16, s_bf16;
   bool unit_scale;        // no scales: every group scale is 1 (scales unused)
   int sym_zero;           // zero of every group when zeros == nullptr
+  long long wait_limit;   // few-token kernel: SM cycles after which a barrier wait gives up
+  int withhold;           // few-token kernel test hook: ring stage never filled (-1: none)
   uint32_t *err;          // device status word
 };
 
