@@ -225,3 +225,43 @@ def test_cluster_split_needs_no_workspace():
     d = to_device(p)
     y = run(p, d).cpu().numpy()
     assert_close(y, oracle_y(p), p.K, p.name)
+
+
+PERSIST = [  # (M, K, N, x dtype): few tiles, so persistent CTAs with stream-K shares
+    (256, 4096, 256, "bf16"),    # one tile, two CTAs
+    (300, 4096, 1024, "bf16"),   # 8 tiles (two token tiles), 16 CTAs
+    (1024, 4096, 1024, "f16"),   # 16 tiles, 32 CTAs
+    (700, 8192, 2304, "bf16"),   # 27 tiles, 54 CTAs: shares cut tiles at odd stages
+    (130, 1024, 128, "f16"),     # one 128-token tile (one accumulator), 16 stages
+]
+
+
+@pytest.mark.parametrize("M,K,N,xd", PERSIST)
+def test_prefill_persistent_shares_match_one_tile_per_cta(M, K, N, xd):
+    # the many-token kernel with a workspace runs persistent (stream-K shares,
+    # cut tiles finished by a fix-up); without one, one tile per CTA.  Both
+    # must match the oracle, and each other bit for bit on integer-exact data.
+    for exact in (False, True):
+        p = syn.grouped("persist", M, K, N, 4, 128, xd, xd, (0.002, 0.02), seed=M + N, int_exact=exact)
+        assert wq.wq_matmul_path(M, K, 4, 128, p.x.dtype, p.scales.dtype) == 2
+        d = to_device(p)
+        need = wq.wq_workspace_bytes(M, N, K, 4, 128)
+        ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+        y_sk = wq.wq_matmul(d["x"], d["packed"], d["scales"], d["zeros"], M, N, K, 4, 128, workspace=ws)
+        y_sk2 = wq.wq_matmul(d["x"], d["packed"], d["scales"], d["zeros"], M, N, K, 4, 128, workspace=ws)
+        tiny = torch.zeros(16, dtype=torch.uint8, device="cuda")
+        y_dp = wq.wq_matmul(d["x"], d["packed"], d["scales"], d["zeros"], M, N, K, 4, 128, workspace=tiny)
+        wq.wq_check_device()
+        assert need > 16384  # the persistent kernel has its partial tiles
+        assert torch.equal(y_sk, y_sk2)  # deterministic
+        assert int(ws[:16384].count_nonzero()) == 0  # flags back at zero
+        if exact:
+            assert torch.equal(y_sk, y_dp)
+        rows = sorted(set([0, M - 1] + np.random.default_rng(M).choice(M, size=min(M, 30), replace=False).tolist()))
+        ref = oracle_y(p, rows=rows)
+        for y in (y_sk, y_dp):
+            yy = y.cpu().numpy()[rows]
+            if exact:
+                assert np.array_equal(yy.astype(np.float64), ref)
+            else:
+                assert_close(yy, ref, K, "persistent %s" % ((M, K, N, xd),))

@@ -141,9 +141,10 @@ Route route_of(const MatmulArgs &a) {
   return Route::kMidm;
 }
 
-wq_status run_call(const Call &c, void *workspace, void *stream) {
+wq_status run_call(const Call &c, void *workspace, size_t workspace_bytes, void *stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (c.route == Route::kPrefill) return launch_prefill(c.a, s) == cudaSuccess ? WQ_OK : WQ_ERR_CUDA;
+  if (c.route == Route::kPrefill)
+    return launch_prefill(c.a, c.sms, workspace, workspace_bytes, s) == cudaSuccess ? WQ_OK : WQ_ERR_CUDA;
   if (c.route == Route::kMidm) {
     const MidmPlan pl = plan_midm(c.a.M, c.a.N, c.a.K, c.sms);
     return launch_midm(c.a, pl, s) == cudaSuccess ? WQ_OK : WQ_ERR_CUDA;
@@ -229,7 +230,11 @@ size_t wq_workspace_bytes(int M, int N, int K, int w_bit, int group_size) {
   a.K = K;
   a.w_bit = w_bit;
   a.group_size = group_size;
-  if (wq::route_of(a) != wq::Route::kDecode) return 0;
+  // The tensor-core paths need no workspace; with this much the many-token
+  // kernel (int4, same x and scale dtype) runs persistent.  Which of them a
+  // call takes depends on its dtypes, so this covers either.
+  if (wq::route_of(a) != wq::Route::kDecode)
+    return (w_bit == 4 && wq::kPrefillMinM <= M) ? wq::prefill_workspace_bytes(M, N, K, d->sms) : 0;
   // Enough with zeros or without (the zero rows' shared memory can change the split).
   const size_t with_z = slice_workspace(M, N, K, w_bit, group_size, true, d->sms);
   const size_t without = w_bit == 8 ? with_z : slice_workspace(M, N, K, w_bit, group_size, false, d->sms);
@@ -243,11 +248,9 @@ wq_status wq_matmul_ex(const void *x, wq_dtype x_dtype, const void *packed_w, co
   wq_status st = wq::prepare_call(x, x_dtype, packed_w, scales, s_dtype, zeros, M, N, K, w_bit, group_size, out,
                                   out_dtype, &c);
   if (st != WQ_OK || c.noop) return st;
-  if (c.need > 0) {
-    if (!workspace || workspace_bytes < c.need) return WQ_ERR_WORKSPACE;
-    if (!aligned(workspace, 16)) return WQ_ERR_ALIGN;
-  }
-  return wq::run_call(c, workspace, stream);
+  if (c.need > 0 && (!workspace || workspace_bytes < c.need)) return WQ_ERR_WORKSPACE;
+  if (workspace && !aligned(workspace, 16)) return WQ_ERR_ALIGN;
+  return wq::run_call(c, workspace, workspace ? workspace_bytes : 0, stream);
 }
 
 wq_status wq_matmul(const void *x, wq_dtype x_dtype, const void *packed_w, const void *scales, wq_dtype s_dtype,
@@ -343,7 +346,7 @@ wq_status wq_t2_matmul(const int8_t *x, const void *packed_w, int M, int N, int 
   c.sms = d->sms;
   c.route = wq::Route::kDecode;
   c.need = dec;
-  return wq::run_call(c, dec > 0 ? workspace : nullptr, stream);
+  return wq::run_call(c, workspace, xoff, stream);
 }
 
 int wq_matmul_path(int M, int K, int w_bit, int group_size, wq_dtype x_dtype, wq_dtype s_dtype) {

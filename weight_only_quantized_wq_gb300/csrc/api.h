@@ -36,7 +36,8 @@ wq_status prepare_call(const void *x, wq_dtype x_dtype, const void *packed_w, co
                        wq_dtype out_dtype, Call *c);
 
 // Enqueue the kernels of a prepared call on `stream`; workspace holds at
-// least c.need bytes (zero-filled counters) when c.need > 0.
-wq_status run_call(const Call &c, void *workspace, void *stream);
+// least c.need bytes (zero-filled counters) when c.need > 0, and
+// workspace_bytes in all (more lets the many-token kernel run persistent).
+wq_status run_call(const Call &c, void *workspace, size_t workspace_bytes, void *stream);
 
 }  // namespace wq

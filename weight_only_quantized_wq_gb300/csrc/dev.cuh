@@ -98,6 +98,25 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_
   }
 }
 
+// mbar_wait for threads with nothing else to do for a long time (an epilogue
+// waiting for a whole K range): between tests the thread sleeps, so it takes
+// no issue slots from the warps doing the work.  Same limit and abort rules.
+__device__ __forceinline__ bool mbar_wait_idle(uint32_t bar, uint32_t parity, uint32_t *err, volatile int *abort,
+                                               unsigned sleep_ns = 256) {
+  if (mbar_test_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  for (;;) {
+    __nanosleep(sleep_ns);
+    if (mbar_test_wait(bar, parity)) return true;
+    if (abort && *abort) return false;
+    if (clock64() - t0 > kWaitLimitCycles) {
+      atomicOr(err, kDevErrTimeout);
+      if (abort) *abort = 1;
+      return false;
+    }
+  }
+}
+
 // ---------------------------------------------------------------- bulk copy
 // L2 policy: weights are read exactly once per call; let them go first.
 __device__ __forceinline__ uint64_t policy_evict_first() {

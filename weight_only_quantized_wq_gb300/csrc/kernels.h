@@ -74,7 +74,13 @@ cudaError_t launch_decode(const MatmulArgs &a, const DecodePlan &p, void *worksp
 // Tensor-core path for many tokens (int4 codes, group size a multiple of 64,
 // scales in the x dtype).
 bool prefill_supported(const MatmulArgs &a);
-cudaError_t launch_prefill(const MatmulArgs &a, cudaStream_t s);
+// Workspace with which the many-token kernel runs persistent with stream-K
+// shares (flags, then one fp32 partial tile per CTA), for problems with at
+// most a quarter as many tiles as SMs (0 otherwise); with less it runs one
+// tile per CTA.
+// The flags share the workspace's zero-filled counter region.
+size_t prefill_workspace_bytes(int M, int N, int K, int sms);
+cudaError_t launch_prefill(const MatmulArgs &a, int sms, void *workspace, size_t workspace_bytes, cudaStream_t s);
 
 // Tensor-core path for a moderate number of tokens (int4 codes, group size
 // a multiple of 64): exact weights, group scales applied in fp32.

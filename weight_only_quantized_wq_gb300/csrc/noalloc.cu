@@ -46,6 +46,13 @@ wq_status scratch_for_current_device(void **out) {
   return WQ_OK;
 }
 
+// Scratch bytes a call may use: the whole array when it needs scratch (the
+// many-token kernel never gets it: its persistent mode needs more partial
+// tiles than the array holds, and one tile per CTA needs none).
+size_t need_scratch_bytes(const wq::Call &c) {
+  return c.need > 0 ? kNoAllocScratchBytes : 0;
+}
+
 }  // namespace
 
 extern "C" {
@@ -67,7 +74,7 @@ wq_status wq_matmul_noalloc(const void *x, wq_dtype x_dtype, const void *packed_
     if (cudaMemsetAsync(scratch, 0, wq::decode_counter_bytes(), static_cast<cudaStream_t>(stream)) != cudaSuccess)
       return WQ_ERR_CUDA;
   }
-  return wq::run_call(c, scratch, stream);
+  return wq::run_call(c, scratch, need_scratch_bytes(c), stream);
 }
 
 }  // extern "C"

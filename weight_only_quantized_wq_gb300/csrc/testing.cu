@@ -23,7 +23,7 @@ wq_status wq_testing_decode_timeout(const void *x, wq_dtype x_dtype, const void 
   if (c.need > 0 && (!workspace || workspace_bytes < c.need)) return WQ_ERR_WORKSPACE;
   c.a.wait_limit = wait_limit_cycles;
   c.a.withhold = withhold_stage;
-  return wq::run_call(c, workspace, stream);
+  return wq::run_call(c, workspace, workspace_bytes, stream);
 }
 
 }  // extern "C"
