@@ -209,8 +209,10 @@ WQ_API wq_status wq_matmul_ex(const void *x, wq_dtype x_dtype, const void *packe
  * Same arguments and result as wq_matmul, without the workspace.  Its scratch
  * is a fixed 8 MiB array inside the library image that every GPU which loads
  * the library keeps until the process exits; no call allocates or frees
- * anything.  A problem whose wq_workspace_bytes() exceeds 8 MiB returns
- * WQ_ERR_WORKSPACE (use wq_matmul with a workspace instead).
+ * anything.  A problem on the few-token kernel (wq_matmul_path 0) whose
+ * wq_workspace_bytes() exceeds 8 MiB returns WQ_ERR_WORKSPACE (use wq_matmul
+ * with a workspace instead); the tensor-core kernels need no scratch here (the
+ * many-token kernel runs one tile per thread block).
  *  - The first call on a device (made with that device current) looks up the
  *    array's device address; make that first call before any stream capture.
  *  - All calls share the one array and it keeps the previous call's
