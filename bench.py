@@ -538,9 +538,16 @@ def main():
         import oracle
         oracle.build()
         p = get_problem(args)
-        steps = max(1, min(args.steps, 20))
-        warm = max(0, min(args.warmup, 3))
-        gbps, cores, sample, dt = cpu_measure(p, steps, warm)
+        steps, warm = max(1, args.steps), max(0, args.warmup)
+        # Exactly the requested steps, each a column sample of the workload sized
+        # so that the whole run takes about two minutes of host time.
+        threads = os.cpu_count() or 1
+        t0 = time.perf_counter()
+        oracle_step(p, p.N, threads)
+        full = time.perf_counter() - t0
+        per_step = 120.0 / (steps + warm)
+        ncols = max(16, min(p.N, int(p.N * per_step / full) // 16 * 16))
+        gbps, cores, sample, dt = cpu_measure(p, steps, warm, ncols=ncols)
         line = {"impl": "reference", "metric": METRIC, "value": round(gbps, 3), "unit": UNIT, "n_gpus": args.gpus,
                 "steps": steps, "warmup": warm, "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
@@ -612,11 +619,11 @@ def main():
             "warmup": args.warmup, "ms_per_step": round(per_step * 1e3, 5), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if hasattr(p, "w_bit") else "int8",
             "data": "synthetic",
-            "config": config_of(p, {"parallelism": "replicas" if world > 1 else "single GPU",
-                                    "l2": "rotating %d buffer sets, %.0f MB total > 3x L2 (%.0f MB)" % (
-                                        len(b.sets), len(b.sets) * b.total_bytes() / 1e6, l2 / 1e6),
-                                    "tflops": round(p.flops * args.steps / sec / 1e12, 3)},
-                                out={"f32": "fp32", "f16": "fp16", "bf16": "bf16"}[args.out_dtype]),
+            "config": config_of(p, out={"f32": "fp32", "f16": "fp16", "bf16": "bf16"}[args.out_dtype]),
+            "timing": {"parallelism": "replicas" if world > 1 else "single GPU",
+                       "l2": "rotating %d buffer sets, %.0f MB total > 3x L2 (%.0f MB)" % (
+                           len(b.sets), len(b.sets) * b.total_bytes() / 1e6, l2 / 1e6),
+                       "tflops": round(p.flops * args.steps / sec / 1e12, 3)},
             "roofline": roof,
             "e2e": e2e,
             "gpu_launches": args.steps * lpc,

@@ -42,6 +42,27 @@ def test_noalloc_matches_workspace_entry_point_twice(make):
         assert_close(y, y_oracle, p.K, "noalloc vs oracle %s" % p.name)
 
 
+def test_noalloc_many_token_problem_runs_one_tile_per_block():
+    # a many-token problem with few tiles: with a workspace wq_matmul runs the
+    # persistent stream-K kernel; without allocation, one tile per thread block
+    # (no scratch).  Same result within the tolerance, bit for bit on
+    # integer-exact data, and the oracle's.
+    for exact in (False, True):
+        p = syn.grouped("prefill noalloc", 300, 4096, 512, 4, 128, "bf16", "bf16", (0.002, 0.02), seed=9,
+                        int_exact=exact)
+        assert wq.wq_matmul_path(p.M, p.K, 4, 128, p.x.dtype, p.scales.dtype) == 2
+        d = to_device(p)
+        ref = wq.wq_matmul(d["x"], d["packed"], d["scales"], d["zeros"], p.M, p.N, p.K, 4, 128)
+        out = torch.full((p.M, p.N), float("nan"), device="cuda")
+        wq.wq_matmul_noalloc(d["x"], d["packed"], d["scales"], d["zeros"], p.M, p.N, p.K, 4, 128, out=out)
+        wq.wq_check_device()
+        if exact:
+            assert torch.equal(out, ref)
+        assert_close(out.cpu().numpy(), ref.cpu().numpy().astype(np.float64), p.K, "noalloc vs wq_matmul")
+        rows = [0, 77, 150, 299]
+        assert_close(out.cpu().numpy()[rows], oracle_y(p, rows=rows), p.K, "noalloc vs oracle")
+
+
 def test_noalloc_scratch_is_used_by_a_split_problem():
     # the narrow problem splits K too finely for a cluster, so the scratch path really runs
     p = _narrow()
