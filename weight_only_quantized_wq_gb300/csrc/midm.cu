@@ -227,7 +227,8 @@ __global__ void __launch_bounds__(THREADS, midm_min_blocks(NT)) midm_kernel(cons
     const int q = (wi + 2) & 3;  // TMEM lane quarter this warp may read (warp index mod 4)
     const int hf = wi >> 2;      // which half of the token columns it folds
     const int tile = wi;         // 16-channel tile it dequantizes
-    const int gq = lane >> 2, tq = lane & 3;
+    const int slot = tc::dq_slot(lane);  // this lane's 16-byte slot of a tile chunk
+    const int gq = slot >> 2, tq = slot & 3;
     constexpr uint32_t MAGIC_LO = Magic<BF16>::kPair & 0xFFFFu;
     float acc[HALF];
 #pragma unroll
@@ -315,7 +316,7 @@ __global__ void __launch_bounds__(THREADS, midm_min_blocks(NT)) midm_kernel(cons
         ++g;
       }
       uint4 wv = make_uint4(0u, 0u, 0u, 0u);
-      if (tile < ntiles) wv = lds128(base + tile * 512 + lane * 16);
+      if (tile < ntiles) wv = lds128(base + tile * 512 + slot * 16);
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_addr(&wempty[ws]));  // the weight slot may be refilled
       if (tile < ntiles) {

@@ -295,7 +295,7 @@ __global__ void __launch_bounds__(SK_THREADS, 1) prefill_sk_kernel(const __grid_
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
           const int pr = dq + half * 256;  // (tile, lane) pair 0..511
-          const int tile = pr >> 5, ln = pr & 31;
+          const int tile = pr >> 5, ln = tc::dq_slot(pr & 31);
           if (tile < ntiles) {
             const uint4 wv = lds128(base + ST_W + tile * 512 + ln * 16);
             const int gq = ln >> 2, tq = ln & 3;
@@ -546,7 +546,7 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         const int pr = dq + half * 256;  // (tile, lane) pair 0..511
-        const int tile = pr >> 5, ln = pr & 31;
+        const int tile = pr >> 5, ln = tc::dq_slot(pr & 31);
         if (tile < ntiles) {
           const uint4 wv = lds128(base + ST_W + tile * 512 + ln * 16);
           const int gq = ln >> 2, tq = ln & 3;

@@ -91,5 +91,18 @@ __device__ __forceinline__ uint32_t sw128_off(int r, int k) {
   return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((((k * 2) >> 4) ^ (r & 7)) << 4) + ((k * 2) & 15));
 }
 
+// Which 16-byte lane slot of a packed 16-channel tile chunk (512 bytes) lane
+// l of a dequantizing warp takes.  Slot j holds rows j/4 and j/4 + 8 and the
+// k quads j%4 of each 16-k step; its 8-byte runs land in a 128-byte-swizzled
+// tile at chunk (c + (j%4)/2) ^ row.  With slot j = l, the 16 lanes of a half
+// warp cover rows 0..3 only and two of them hit every bank pair (4 wavefronts
+// per 8-byte store); this bijection gives each half warp all eight rows, one
+// run per bank pair (2 wavefronts), while each quarter warp still reads eight
+// distinct 16-byte bank groups of the chunk.
+__device__ __forceinline__ int dq_slot(int l) {
+  const int q = l >> 3, b = l & 7;
+  return (((q + 2 * (b >> 2)) & 3) << 3) | b;
+}
+
 }  // namespace tc
 }  // namespace wq
