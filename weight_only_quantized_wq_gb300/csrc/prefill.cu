@@ -28,7 +28,7 @@
 // one fix-up per cut tile.  The launch is cooperative (all CTAs resident),
 // so the waits cannot deadlock.  Without a workspace that holds the partial
 // tiles, one tile per CTA runs.
-// Roles of the persistent kernel (14 warps; the one-tile kernel has warps 0..9):
+// Roles of the persistent kernel (14 warps):
 //   warp 0       producer: per stage one TMA copy of the x tile (256 x 64,
 //                128-byte swizzle), one 1-D bulk copy of the packed weights
 //                (256 channels x 64 k), TMA copies of the scale and zero rows
@@ -39,6 +39,10 @@
 //   warps 10..13 epilogue: tcgen05.ld of the fp32 accumulator (one token row
 //                per thread), then partial, fix-up or store; the next run of
 //                stages starts as soon as the accumulator is read out.
+// Roles of the one-tile kernel (11 warps): warp 0 x producer (its own ring
+// of x tiles), warp 1 TMEM and the MMA issuer, warp 2 weight producer (a
+// short ring of packed weights, scale and zero rows), warps 3..10 dequant,
+// of which 4..7 read the accumulator out at the end.
 // The scale and zero are applied to the weight (one rounding to bf16/fp16),
 // since a per-group rescale of a 128 x 256 TMEM accumulator would cost more
 // than the tensor cores gain; calls where that rounding could exceed the
@@ -63,7 +67,7 @@ constexpr int STAGES = 3;
 constexpr int BSTAGES = 2;            // dequantized B buffers
 constexpr int DQ_WARPS = 8;
 constexpr int EPI_WARPS = 4;
-constexpr int THREADS = (2 + DQ_WARPS) * 32;                 // one tile per CTA
+constexpr int THREADS = (3 + DQ_WARPS) * 32;                 // one tile per CTA
 constexpr int SK_THREADS = (2 + DQ_WARPS + EPI_WARPS) * 32;  // persistent, stream-K
 constexpr int B_BYTES = BN * BK * 2;  // 32 KB
 constexpr int W_BYTES = BN * BK / 2;  // 8 KB of packed int4
@@ -83,6 +87,29 @@ struct Cfg {
   static constexpr int STAGE_BYTES = (ST_Z + Z_BYTES + 1023) / 1024 * 1024;
   static constexpr int SMEM = HEADER + STAGES * STAGE_BYTES + BSTAGES * B_BYTES;
   static constexpr int TMEM_COLS = BN * MS;           // 256 or 512
+};
+
+// Geometry of the one-tile kernel, whose x tiles and weight rows travel in
+// separate rings.  An x tile must stay until the MMAs of its stage have read
+// it; a weight slot only until the dequant warps hold its words in
+// registers.  So the weights run ahead on a short ring of their own and the
+// x ring's depth is spent on the x tiles' own latency alone (in one shared
+// ring every slot was held for that latency plus the dequant plus the MMAs).
+template <int MS>
+struct DCfg {
+  static constexpr int MSUB = MS;
+  static constexpr int BM = UM * MS;                           // tokens per tile
+  static constexpr int A_BYTES = BM * BK * 2;                  // x tile: 16 or 32 KB
+  static constexpr int XS = MS == 2 ? 4 : 7;                   // x tiles in the ring
+  static constexpr int WS = 3;                                 // weight slots
+  static constexpr int W_SLOT = W_BYTES + S_BYTES + Z_BYTES;   // packed weights | scale row | zero row
+  static constexpr int OFF_X = HEADER;                         // 1024-byte aligned (swizzle atoms)
+  static constexpr int OFF_B = OFF_X + XS * A_BYTES;
+  static constexpr int OFF_W = OFF_B + BSTAGES * B_BYTES;
+  static constexpr int SMEM = OFF_W + WS * W_SLOT;
+  static constexpr int TMEM_COLS = BN * MS;                    // 256 or 512
+  static_assert(W_SLOT % 128 == 0, "weight slots keep 128-byte alignment");
+  static_assert((2 * (XS + WS + BSTAGES) + 1) * 8 + 8 <= HEADER, "barriers do not fit the header");
 };
 
 struct Params {
@@ -443,21 +470,24 @@ __global__ void __launch_bounds__(SK_THREADS, 1) prefill_sk_kernel(const __grid_
 // 4..7 read the accumulator out after their share of the dequant.
 template <bool BF16, bool ZERO, int MS>
 __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_constant__ Params p) {
-  using C = Cfg<MS>;
-  constexpr int MSUB = C::MSUB, BM = C::BM, A_BYTES = C::A_BYTES, STAGE_BYTES = C::STAGE_BYTES;
-  constexpr int ST_A = C::ST_A, ST_W = C::ST_W, ST_S = C::ST_S, ST_Z = C::ST_Z, TMEM_COLS = C::TMEM_COLS;
+  using C = DCfg<MS>;
+  constexpr int MSUB = C::MSUB, BM = C::BM, A_BYTES = C::A_BYTES, XS = C::XS, WS = C::WS;
+  constexpr int W_SLOT = C::W_SLOT, TMEM_COLS = C::TMEM_COLS;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte alignment (of the shared-window address) for the swizzled tiles
   uint8_t *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
-  uint64_t *full = reinterpret_cast<uint64_t *>(smem);          // TMA data of a stage landed
-  uint64_t *empty = full + STAGES;                                // MMA done with a stage
-  uint64_t *bfull = empty + STAGES;                               // dequantized B written
-  uint64_t *bempty = bfull + BSTAGES;                             // MMA done with a B buffer
-  uint64_t *accfull = bempty + BSTAGES;                           // accumulator complete
+  uint64_t *xfull = reinterpret_cast<uint64_t *>(smem);  // x tile of a stage landed
+  uint64_t *xempty = xfull + XS;                          // MMAs done with an x tile
+  uint64_t *wfull = xempty + XS;                          // weight rows of a stage landed
+  uint64_t *wempty = wfull + WS;                          // every dequant warp holds them in registers
+  uint64_t *bfull = wempty + WS;                          // dequantized B written
+  uint64_t *bempty = bfull + BSTAGES;                     // MMA done with a B buffer
+  uint64_t *accfull = bempty + BSTAGES;                   // accumulator complete
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(accfull + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-  uint8_t *ring = smem + HEADER;
-  uint8_t *bbuf = ring + STAGES * STAGE_BYTES;
+  uint8_t *xring = smem + C::OFF_X;
+  uint8_t *bbuf = smem + C::OFF_B;
+  uint8_t *wring = smem + C::OFF_W;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // Token tiles vary fastest across the grid, so the CTAs that read the same
@@ -469,9 +499,13 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
   const int nk = p.K / BK;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < STAGES; ++i) {
-      mbar_init(smem_addr(&full[i]), 1);
-      mbar_init(smem_addr(&empty[i]), 1);
+    for (int i = 0; i < XS; ++i) {
+      mbar_init(smem_addr(&xfull[i]), 1);
+      mbar_init(smem_addr(&xempty[i]), 1);
+    }
+    for (int i = 0; i < WS; ++i) {
+      mbar_init(smem_addr(&wfull[i]), 1);
+      mbar_init(smem_addr(&wempty[i]), DQ_WARPS);
     }
     for (int i = 0; i < BSTAGES; ++i) {
       mbar_init(smem_addr(&bfull[i]), DQ_WARPS);
@@ -490,82 +524,116 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
-    // ------------------------------------------------------------ producer
+    // ------------------------------------------------------------ x producer
+    if (lane == 0) {
+      int issued = 0;
+      for (int i = 0; i < nk; ++i) {
+        const int s = i % XS;
+        if (i >= XS && !mbar_wait(smem_addr(&xempty[s]), ((i / XS) - 1) & 1, p.err, abort_flag)) break;
+        const uint32_t fb = smem_addr(&xfull[s]);
+        mbar_arrive_expect_tx(fb, A_BYTES);
+        tma_load_2d(smem_addr(xring + s * A_BYTES), &p.tm_x, i * BK, m0, fb);
+        issued = i + 1;
+      }
+      // No copy may still be writing this CTA's shared memory when it exits.
+      for (int i = max(0, issued - XS); i < issued; ++i)
+        mbar_wait(smem_addr(&xfull[i % XS]), (i / XS) & 1, p.err, nullptr);
+    }
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ weight producer
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
       int issued = 0;
       for (int i = 0; i < nk; ++i) {
-        const int st = i % STAGES;
-        if (i >= STAGES && !mbar_wait(smem_addr(&empty[st]), ((i / STAGES) - 1) & 1, p.err, abort_flag)) break;
-        const uint32_t fb = smem_addr(&full[st]);
-        const uint32_t base = smem_addr(ring + st * STAGE_BYTES);
+        const int s = i % WS;
+        if (i >= WS && !mbar_wait(smem_addr(&wempty[s]), ((i / WS) - 1) & 1, p.err, abort_flag)) break;
+        const uint32_t fb = smem_addr(&wfull[s]);
+        const uint32_t base = smem_addr(wring + s * W_SLOT);
         const int g = i * BK / p.gs;
-        mbar_arrive_expect_tx(fb, A_BYTES + ntiles * 512 + S_BYTES + (ZERO ? Z_BYTES : 0));
-        tma_load_2d(base + ST_A, &p.tm_x, i * BK, m0, fb);
-        bulk_g2s(base + ST_W, p.packed + ((size_t)i * p.nt_total + nt0) * 512, ntiles * 512, fb, pol);
-        tma_load_2d(base + ST_S, &p.tm_s, n0, g, fb);
-        if (ZERO) tma_load_2d(base + ST_Z, &p.tm_z, n0, g / 8, fb);
+        mbar_arrive_expect_tx(fb, ntiles * 512 + S_BYTES + (ZERO ? Z_BYTES : 0));
+        bulk_g2s(base, p.packed + ((size_t)i * p.nt_total + nt0) * 512, ntiles * 512, fb, pol);
+        tma_load_2d(base + W_BYTES, &p.tm_s, n0, g, fb);
+        if (ZERO) tma_load_2d(base + W_BYTES + S_BYTES, &p.tm_z, n0, g / 8, fb);
         issued = i + 1;
       }
-      for (int i = max(0, issued - STAGES); i < issued; ++i)
-        mbar_wait(smem_addr(&full[i % STAGES]), (i / STAGES) & 1, p.err, nullptr);
+      for (int i = max(0, issued - WS); i < issued; ++i)
+        mbar_wait(smem_addr(&wfull[i % WS]), (i / WS) & 1, p.err, nullptr);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t id = tc::idesc<BF16>(UM, BN);
       for (int i = 0; i < nk; ++i) {
-        const int st = i % STAGES, sb = i % BSTAGES;
-        if (!mbar_wait(smem_addr(&full[st]), (i / STAGES) & 1, p.err, abort_flag)) break;
+        const int s = i % XS, sb = i % BSTAGES;
         if (!mbar_wait(smem_addr(&bfull[sb]), (i / BSTAGES) & 1, p.err, abort_flag)) break;
+        if (!mbar_wait(smem_addr(&xfull[s]), (i / XS) & 1, p.err, abort_flag)) break;
         tc::fence_after();
-        const uint32_t a0 = smem_addr(ring + st * STAGE_BYTES + ST_A);
+        const uint32_t a0 = smem_addr(xring + s * A_BYTES);
         const uint32_t b0 = smem_addr(bbuf + sb * B_BYTES);
 #pragma unroll
         for (int h = 0; h < MSUB; ++h)
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk)
             tc::mma(tmem + h * BN, tc::sw128_desc(a0 + h * (UM * 128) + kk * 32), tc::sw128_desc(b0 + kk * 32), id,
-                 (i | kk) != 0 ? 1u : 0u);
-        tc::commit(smem_addr(&empty[st]));
+                    (i | kk) != 0 ? 1u : 0u);
+        tc::commit(smem_addr(&xempty[s]));
         tc::commit(smem_addr(&bempty[sb]));
       }
       tc::commit(smem_addr(accfull));  // every MMA issued above has completed when this fires
     }
   } else {
-    // ------------------------------------------------------------ dequant (warps 2..9)
-    const int dq = threadIdx.x - 64;  // 0 .. 255
+    // ------------------------------------------------------------ dequant (warps 3..10)
+    const int dq = threadIdx.x - 96;  // 0 .. 255
     constexpr uint32_t MAGIC = Magic<BF16>::kPair;
     for (int i = 0; i < nk; ++i) {
-      const int st = i % STAGES, sb = i % BSTAGES;
-      if (!mbar_wait(smem_addr(&full[st]), (i / STAGES) & 1, p.err, abort_flag)) break;
-      if (i >= BSTAGES && !mbar_wait(smem_addr(&bempty[sb]), ((i / BSTAGES) - 1) & 1, p.err, abort_flag)) break;
-      const uint32_t base = smem_addr(ring + st * STAGE_BYTES);
-      const uint32_t bdst = smem_addr(bbuf + sb * B_BYTES);
+      const int s = i % WS, sb = i % BSTAGES;
+      if (!mbar_wait(smem_addr(&wfull[s]), (i / WS) & 1, p.err, abort_flag)) break;
+      const uint32_t base = smem_addr(wring + s * W_SLOT);
       const int g = i * BK / p.gs;
+      // This thread's words, scales and zeros of the stage into registers;
+      // then the weight slot goes back to the producer.
+      uint4 wv[2];
+      uint32_t zz[2][2], ss[2][2];
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         const int pr = dq + half * 256;  // (tile, lane) pair 0..511
         const int tile = pr >> 5, ln = tc::dq_slot(pr & 31);
+        wv[half] = make_uint4(0u, 0u, 0u, 0u);
         if (tile < ntiles) {
-          const uint4 wv = lds128(base + ST_W + tile * 512 + ln * 16);
-          const int gq = ln >> 2, tq = ln & 3;
-          const uint32_t w4[4] = {wv.x, wv.y, wv.z, wv.w};
+          wv[half] = lds128(base + tile * 512 + ln * 16);
 #pragma unroll
           for (int r = 0; r < 2; ++r) {
-            const int col = tile * 16 + gq + 8 * r;  // row of B (output channel within the tile)
-            const uint16_t sbits = lds16(base + ST_S + col * 2);
+            const int col = tile * 16 + (ln >> 2) + 8 * r;  // row of B (output channel within the tile)
+            const uint16_t sbits = lds16(base + W_BYTES + col * 2);
             uint32_t z = 8;
-            if (ZERO) z = (lds32(base + ST_Z + col * 4) >> ((g % 8) * 4)) & 15u;
-            const uint32_t zz = ((MAGIC & 0xFFFFu) + z) * 0x00010001u;  // (MAGIC + z) in both halves
-            const uint32_t ss = (uint32_t)sbits * 0x00010001u;
+            if (ZERO) z = (lds32(base + W_BYTES + S_BYTES + col * 4) >> ((g % 8) * 4)) & 15u;
+            zz[half][r] = ((MAGIC & 0xFFFFu) + z) * 0x00010001u;  // (MAGIC + z) in both halves
+            ss[half][r] = (uint32_t)sbits * 0x00010001u;
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&wempty[s]));
+      if (i >= BSTAGES && !mbar_wait(smem_addr(&bempty[sb]), ((i / BSTAGES) - 1) & 1, p.err, abort_flag)) break;
+      const uint32_t bdst = smem_addr(bbuf + sb * B_BYTES);
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const int pr = dq + half * 256;
+        const int tile = pr >> 5, ln = tc::dq_slot(pr & 31);
+        if (tile < ntiles) {
+          const int gq = ln >> 2, tq = ln & 3;
+          const uint32_t w4[4] = {wv[half].x, wv[half].y, wv[half].z, wv[half].w};
+#pragma unroll
+          for (int r = 0; r < 2; ++r) {
+            const int col = tile * 16 + gq + 8 * r;
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
               const uint32_t w = w4[2 * u + r];
 #pragma unroll
               for (int j = 0; j < 2; ++j) {
-                const uint32_t lo = mul2<BF16>(sub_pair<BF16>(code_pair<4, BF16>(w, 2 * j), zz), ss);
-                const uint32_t hi = mul2<BF16>(sub_pair<BF16>(code_pair<4, BF16>(w, 2 * j + 1), zz), ss);
+                const uint32_t lo = mul2<BF16>(sub_pair<BF16>(code_pair<4, BF16>(w, 2 * j), zz[half][r]), ss[half][r]);
+                const uint32_t hi =
+                    mul2<BF16>(sub_pair<BF16>(code_pair<4, BF16>(w, 2 * j + 1), zz[half][r]), ss[half][r]);
                 const int k = 32 * u + 16 * j + 4 * tq;
                 sts64(bdst + tc::sw128_off(col, k), lo, hi);
               }
@@ -624,7 +692,8 @@ static cudaError_t launch_t(const pf::Params &pp, dim3 grid, bool persistent, cu
   static int attr_set[64][2] = {{0}};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  const int smem = pf::Cfg<MS>::SMEM + 1024;  // + slack for the 1024-byte alignment of the ring
+  // + slack for the 1024-byte alignment of the rings
+  const int smem = (persistent ? pf::Cfg<MS>::SMEM : pf::DCfg<MS>::SMEM) + 1024;
   if (!attr_set[dev][persistent]) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
