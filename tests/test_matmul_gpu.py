@@ -138,6 +138,30 @@ def test_integer_exact_bitwise(case):
     assert np.array_equal(y, ref), "max diff %g" % np.max(np.abs(y - ref))
 
 
+ONE_TILE_RAGGED = [  # (M, K, N, x dtype, integer-exact): many tiles (one per CTA), token and channel tails
+    (300, 4096, 10000, "bf16", False),   # 2 x 40 tiles; the last channel block holds 16 channels
+    (1000, 4096, 6160, "f16", False),    # 4 x 25 tiles
+    (520, 4096, 9744, "bf16", True),     # 3 x 39 tiles, integer-exact: bit for bit
+]
+
+
+@pytest.mark.parametrize("M,K,N,xd,exact", ONE_TILE_RAGGED)
+def test_prefill_one_tile_ragged(M, K, N, xd, exact):
+    # the many-token one-tile kernel (x ring and weight ring of their own) with
+    # partial token tiles and partial channel blocks, on sampled rows
+    p = syn.grouped("one-tile", M, K, N, 4, 128, xd, xd, (0.002, 0.02), seed=M + N, int_exact=exact)
+    assert wq.wq_matmul_path(M, K, 4, 128, p.x.dtype, p.scales.dtype) == 2
+    assert wq.wq_workspace_bytes(M, N, K, 4, 128) == 0  # enough tiles: one per CTA, no stream-K
+    y = run(p).cpu().numpy().astype(np.float64)
+    rng = np.random.default_rng(M)
+    rows = sorted(set([0, 255, 256, M - 1] + rng.choice(np.arange(M), size=12, replace=False).tolist()))
+    ref = oracle_y(p, rows=rows)
+    if exact:
+        assert np.array_equal(y[rows], ref), "max diff %g" % np.max(np.abs(y[rows] - ref))
+    else:
+        assert_close(y[rows], ref, K, p.name)
+
+
 def test_int8_integer_exact_bitwise():
     p = syn.int8("int8-exact", 16, 4096, 1024, "bf16", (0.001, 0.01), seed=12, int_exact=True)
     y = run(p).cpu().numpy().astype(np.float64)
