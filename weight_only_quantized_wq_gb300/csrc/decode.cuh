@@ -262,6 +262,8 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_min_blocks(MT, TN))
   // fp16 int4 only: 960 - (1024 + zero), the fma addend of the odd fields
   constexpr bool kOddFma = W == 4 && !BF16;
   uint32_t zz16[TN][2];
+  // 2-bit codes: the fma addends -(MAGIC/4 + zero) and -(MAGIC/16 + zero)
+  uint32_t n2[TN][2], n4[TN][2];
   auto set_zeros = [&](int gi) {
 #pragma unroll
     for (int ti = 0; ti < TN; ++ti)
@@ -272,6 +274,10 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_min_blocks(MT, TN))
         else
           zz[ti][rr] = ((Magic<BF16>::kPair & 0xFFFFu) + (uint32_t)p.sym_zero) * 0x00010001u;
         if constexpr (kOddFma) zz16[ti][rr] = sub_pair<false>(kF16NineSixty, zz[ti][rr]);
+        if constexpr (W == 2) {
+          n2[ti][rr] = sub_pair<BF16>(Int2InPlace<BF16>::kMagic3of4, zz[ti][rr]);
+          n4[ti][rr] = sub_pair<BF16>(Int2InPlace<BF16>::kMagic15of16, zz[ti][rr]);
+        }
       }
   };
   // acc += scale[gi] * (sum over group gi); the group sum restarts.
@@ -352,6 +358,11 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_min_blocks(MT, TN))
             a1 = sub_pair<false>(and_or(v8, 0x000F000Fu, Magic<false>::kPair), zz[ti][1]);
             a2 = fma_h2(and_or(v, 0x00F000F0u, Magic<false>::kPair), kF16Sixteenth, zz16[ti][0]);
             a3 = fma_h2(and_or(v8, 0x00F000F0u, Magic<false>::kPair), kF16Sixteenth, zz16[ti][1]);
+          } else if constexpr (W == 2) {
+            a0 = int2_pair<BF16>(wg, 2 * j, zz[ti][0], n2[ti][0], n4[ti][0]);
+            a1 = int2_pair<BF16>(wg8, 2 * j, zz[ti][1], n2[ti][1], n4[ti][1]);
+            a2 = int2_pair<BF16>(wg, 2 * j + 1, zz[ti][0], n2[ti][0], n4[ti][0]);
+            a3 = int2_pair<BF16>(wg8, 2 * j + 1, zz[ti][1], n2[ti][1], n4[ti][1]);
           } else {
             a0 = sub_pair<BF16>(code_pair<W, BF16>(wg, 2 * j), zz[ti][0]);
             a1 = sub_pair<BF16>(code_pair<W, BF16>(wg8, 2 * j), zz[ti][1]);

@@ -300,6 +300,44 @@ __device__ __forceinline__ uint32_t fma_h2(uint32_t a, uint32_t b, uint32_t c) {
 constexpr uint32_t kF16Sixteenth = 0x2C002C00u;  // (1/16, 1/16)
 constexpr uint32_t kF16NineSixty = 0x63806380u;  // (960, 960)
 
+// Both 16-bit halves a * b + c (fp16 or bf16 pairs), one rounding.
+template <bool BF16>
+__device__ __forceinline__ uint32_t fma_pair(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  if constexpr (BF16)
+    asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  else
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+// 2-bit fields taken in place.  Masking the field at bits p..p+1 of each
+// 16-bit half (p = 0, 2, 4: inside the 7 fraction bits of a bf16, and of an
+// fp16) gives MAGIC + 2^p q exactly; (MAGIC + 2^p q) * 2^-p - (MAGIC 2^-p + z)
+// = q - z exactly, in one fma whose addend is built once per group from the
+// (MAGIC + z) pair as (1 - 2^-p) MAGIC - (MAGIC + z).  Three of a word's
+// eight pairs need no shift and three more share one shift by 8.
+template <bool BF16>
+struct Int2InPlace {
+  static constexpr uint32_t kQuarter = BF16 ? 0x3E803E80u : 0x34003400u;    // (1/4, 1/4)
+  static constexpr uint32_t kSixteenth = BF16 ? 0x3D803D80u : 0x2C002C00u;  // (1/16, 1/16)
+  static constexpr uint32_t kMagic3of4 = BF16 ? 0x42C042C0u : 0x62006200u;  // 3/4 MAGIC: 96 or 768
+  static constexpr uint32_t kMagic15of16 = BF16 ? 0x42F042F0u : 0x63806380u;  // 15/16 MAGIC: 120 or 960
+};
+
+// Pair i (0..7) of a word of 2-bit codes (fields i and i + 8 in the low and
+// high halves, as code_pair<2> takes them) as the exact q - zero pair.
+// zz = (MAGIC + z), n2 = -(MAGIC/4 + z), n4 = -(MAGIC/16 + z).
+template <bool BF16>
+__device__ __forceinline__ uint32_t int2_pair(uint32_t w, int i, uint32_t zz, uint32_t n2, uint32_t n4) {
+  using P = Int2InPlace<BF16>;
+  const int s = i == 3 ? 6 : i == 7 ? 14 : i >= 4 ? 8 : 0;  // shift that brings the field into bits 0..5
+  const int pos = (i == 1 || i == 5) ? 2 : (i == 2 || i == 6) ? 4 : 0;
+  const uint32_t v = and_or(s ? w >> s : w, 0x00030003u << pos, Magic<BF16>::kPair);
+  if (pos == 0) return sub_pair<BF16>(v, zz);
+  return fma_pair<BF16>(v, pos == 2 ? P::kQuarter : P::kSixteenth, pos == 2 ? n2 : n4);
+}
+
 // Signed int8 bytes (lo, hi) of a word -> exact fp16/bf16 pair.
 template <bool BF16>
 __device__ __forceinline__ uint32_t int8_pair(uint32_t w, int hi_half) {
