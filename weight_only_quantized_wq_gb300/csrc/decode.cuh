@@ -21,7 +21,9 @@
 //
 // Exact group arithmetic (W = 2, 4): one shift and one LOP3 per pair turn two
 // codes into MAGIC + q (exact in fp16 / bf16) and one subtraction of
-// MAGIC + zero gives q - zero, a small integer, exactly.  The MMA sums
+// MAGIC + zero gives q - zero, a small integer, exactly (2-bit codes: six of
+// a word's eight pairs are masked in place or after one shared shift and
+// fixed by one exact fma; fp16 4-bit codes: the odd fields likewise).  The MMA sums
 // x (q - zero) over one group in fp32 and the group's scale is applied to that
 // sum (one FMA per value): no weight is ever rounded.  int8 codes (W = 8) are
 // converted exactly and the per-channel scale is applied at the end (tiny-llm
