@@ -208,6 +208,26 @@ def test_ragged_shapes(M, K, N, wb, gs):
     assert_close(y, oracle_y(p), K, "ragged %s" % ((M, K, N, wb, gs),))
 
 
+LONG_K = [  # (M, K, N, w_bit, group, x dtype): K = 65536, the most the ternary path accepts
+    (1, 65536, 32, 4, 16, "bf16"),     # 4096 groups: many K splits, partials through the workspace
+    (5, 65536, 48, 2, 64, "f16"),
+    (3, 65536, 16, 8, 65536, "bf16"),  # int8 per channel
+    (300, 65536, 512, 4, 128, "bf16"), # many-token kernel: 1024 stages per tile
+]
+
+
+@pytest.mark.parametrize("M,K,N,wb,gs,xd", LONG_K)
+def test_long_k(M, K, N, wb, gs, xd):
+    if wb == 8:
+        p = syn.int8("int8-long-k", M, K, N, xd, (0.001, 0.01), seed=K + N)
+    else:
+        p = syn.grouped("long-k", M, K, N, wb, gs, xd, xd, (0.002, 0.02), seed=K + N + M)
+    y = run(p).cpu().numpy()
+    rows = sorted(set([0, M // 2, M - 1]))
+    assert_close(y[rows], oracle_y(p, rows=rows), K, "long K %s" % ((M, K, N, wb, gs),))
+    wq.wq_check_device()
+
+
 def test_zero_rows_is_noop_and_canaries():
     p = syn.int4_asym_tiny()
     d = to_device(p)
