@@ -183,8 +183,8 @@ class Bench:
     def path(self) -> int:
         if self.ternary:
             return 0
-        return self.wq.wq_matmul_path(self.p.M, self.p.K, self.p.w_bit, self.p.group_size, self.p.x.dtype,
-                                      self.p.scales.dtype)
+        return self.wq.wq_matmul_path(self.p.M, self.p.N, self.p.K, self.p.w_bit, self.p.group_size,
+                                      self.p.x.dtype, self.p.scales.dtype)
 
     def kernel_name(self) -> str:
         k = self.wq.binding.PATHS[self.path()]

@@ -265,14 +265,17 @@ WQ_API wq_status wq_t2_matmul(const int8_t *x, const void *packed_w, int M, int 
  * 0 the few-token kernel (TMA ring, register dequant, mma.sync, split-K in
  * clusters), 1 the exact tensor-core kernel (tcgen05, q - zero exact, group
  * scale in fp32), 2 the many-token tensor-core kernel (weight rounded once to
- * the x dtype); -1 if wq_matmul would reject the arguments' sizes, w_bit or
- * dtypes.  The split by token count plays the part of tiny-llm's MAX_M
+ * the x dtype), 3 the same kernel with each weight as two terms in the x
+ * dtype (the rounded weight and its rounded residue: bf16 below K = 4096,
+ * where one rounding could exceed the accepted error, on problems with
+ * enough tiles to fill the GPU); -1 if wq_matmul would reject the arguments'
+ * sizes, w_bit or dtypes.  The split by token count plays the part of tiny-llm's MAX_M
  * (kernels/int8_gemv.py: up to 64 rows per call on the few-token kernel,
  * more left to a GEMM) and of Marlin's small- and large-batch thread
  * configurations (aphrodite-engine marlin_cuda_kernel.cu).  No device is
  * touched.
  */
-WQ_API int wq_matmul_path(int M, int K, int w_bit, int group_size, wq_dtype x_dtype, wq_dtype s_dtype);
+WQ_API int wq_matmul_path(int M, int N, int K, int w_bit, int group_size, wq_dtype x_dtype, wq_dtype s_dtype);
 
 /*
  * wq_check_device -- synchronise `stream`, then read and clear the device

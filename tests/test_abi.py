@@ -164,24 +164,34 @@ def test_binding_marshals_to_the_c_abi_and_raises_its_status():
 def test_matmul_path_rules(L):
     # the path is a host decision (no device): few tokens or codes / groups the
     # tensor-core kernels do not take -> 0; int4 with 64-aligned groups -> 1
-    # (exact); many tokens where rounding w once holds the bound -> 2
+    # (exact); many tokens where rounding w once holds the bound -> 2; bf16
+    # below K = 4096 on grids of at least 128 tiles -> 3 (two-term weights)
     F16, BF16, F32 = binding.WQ_F16, binding.WQ_BF16, binding.WQ_F32
     P = binding.wq_matmul_path
-    assert P(16, 8192, 4, 128, BF16, BF16) == 0
-    assert P(64, 8192, 4, 128, BF16, BF16) == 0
-    assert P(65, 8192, 4, 128, BF16, BF16) == 2
-    assert P(4096, 8192, 4, 128, BF16, BF16) == 2
-    assert P(65, 2048, 4, 128, BF16, BF16) == 1     # bf16 below K = 4096: exact path
-    assert P(4096, 512, 4, 128, F16, F16) == 2      # fp16 rounding holds the bound
-    assert P(4096, 8192, 4, 128, F16, BF16) == 1    # scale dtype differs from x
-    assert P(4096, 8192, 4, 32, BF16, BF16) == 0    # group not a multiple of 64
-    assert P(4096, 8192, 2, 64, BF16, BF16) == 0    # int2
-    assert P(64, 4096, 8, -1, BF16, F32) == 0       # int8
-    assert P(100, 4096, 4, -1, BF16, BF16) == 2     # per channel
-    assert P(100, 2048, 4, -1, BF16, BF16) == 1
-    assert P(64, 4096, 3, 128, BF16, BF16) == -1
-    assert P(64, 4096, 4, 48, BF16, BF16) == -1
-    assert P(64, 4096, 8, -1, BF16, BF16) == -1
+    N = 4096
+    assert P(16, N, 8192, 4, 128, BF16, BF16) == 0
+    assert P(64, N, 8192, 4, 128, BF16, BF16) == 0
+    assert P(65, N, 8192, 4, 128, BF16, BF16) == 2
+    assert P(4096, N, 8192, 4, 128, BF16, BF16) == 2
+    assert P(65, N, 2048, 4, 128, BF16, BF16) == 1     # bf16 below K = 4096: exact path
+    assert P(4096, N, 512, 4, 128, F16, F16) == 2      # fp16 rounding holds the bound
+    assert P(4096, N, 8192, 4, 128, F16, BF16) == 1    # scale dtype differs from x
+    assert P(4096, N, 8192, 4, 32, BF16, BF16) == 0    # group not a multiple of 64
+    assert P(4096, N, 8192, 2, 64, BF16, BF16) == 0    # int2
+    assert P(64, N, 4096, 8, -1, BF16, F32) == 0       # int8
+    assert P(100, N, 4096, 4, -1, BF16, BF16) == 2     # per channel
+    assert P(100, N, 2048, 4, -1, BF16, BF16) == 1
+    # two-term weights: ceil(M / 256) * ceil(N / 128) >= 128 tiles and M >= 129
+    assert P(1024, 4096, 2048, 4, 128, BF16, BF16) == 3   # 4 x 32 tiles
+    assert P(768, 4096, 2048, 4, 128, BF16, BF16) == 1    # 3 x 32 tiles
+    assert P(256, 16384, 1024, 4, 128, BF16, BF16) == 3   # 1 x 128 tiles
+    assert P(128, 28672, 2048, 4, 128, BF16, BF16) == 1   # under 129 tokens
+    assert P(1024, 4096, 2048, 4, 128, F16, F16) == 2     # fp16: one rounding holds
+    assert P(64, N, 4096, 3, 128, BF16, BF16) == -1
+    assert P(64, N, 4096, 4, 48, BF16, BF16) == -1
+    assert P(64, N, 4096, 8, -1, BF16, BF16) == -1
+    assert P(64, 24, 4096, 4, 128, BF16, BF16) == -1     # N not a multiple of 16
+    assert P(64, 0, 4096, 4, 128, BF16, BF16) == -1
 
 
 def test_t2_host_validation(L):

@@ -77,7 +77,7 @@ def test_sweep_weights_exact_tensor_core_path(M):
     p = full.rows(M)
     p = p.__class__(**dict(p.__dict__, x=p.x.to(torch.float16), x_dtype="f16"))
     want = 0 if M <= 64 else 1
-    assert wq.wq_matmul_path(M, p.K, 4, p.group_size, torch.float16, torch.bfloat16) == want
+    assert wq.wq_matmul_path(M, p.N, p.K, 4, p.group_size, torch.float16, torch.bfloat16) == want
     y = run(p).cpu().numpy()
     rows = sorted(set([0, M // 2, M - 1]))
     assert_close(y[rows], oracle_y(p, rows=rows), p.K, p.name)
@@ -96,7 +96,7 @@ def test_tensor_core_paths_short_k(M, K, N, gs, xd, sym):
     # bf16 many-token problems below K = 4096 take the exact path (rounding w
     # to bf16 would not hold the bound there); fp16 ones may round w once.
     p = syn.grouped("short-k", M, K, N, 4, gs, xd, xd, (0.002, 0.02), symmetric=sym, seed=M + K + N)
-    path = wq.wq_matmul_path(M, K, 4, gs, p.x.dtype, p.scales.dtype)
+    path = wq.wq_matmul_path(M, N, K, 4, gs, p.x.dtype, p.scales.dtype)
     assert path == (0 if M <= 64 else 2 if xd == "f16" else 1)
     y = run(p).cpu().numpy()
     assert_close(y, oracle_y(p), K, "short K %s" % ((M, K, N, gs, xd, sym),))
@@ -131,7 +131,7 @@ INT_EXACT_PATH = {"int4-asym-bf16-M200": 1, "int4-asym-f16x-bf16s-M70": 1, "int4
 def test_integer_exact_bitwise(case):
     name, M, K, N, wb, gs, xd, sd, sym = case
     dt = {"f16": torch.float16, "bf16": torch.bfloat16}
-    assert wq.wq_matmul_path(M, K, wb, gs, dt[xd], dt[sd]) == INT_EXACT_PATH.get(name, 0)
+    assert wq.wq_matmul_path(M, N, K, wb, gs, dt[xd], dt[sd]) == INT_EXACT_PATH.get(name, 0)
     p = syn.grouped(name, M, K, N, wb, gs, xd, sd, (0, 0), symmetric=sym, seed=11, int_exact=True)
     y = run(p).cpu().numpy().astype(np.float64)
     ref = oracle_y(p)
@@ -150,7 +150,7 @@ def test_prefill_one_tile_ragged(M, K, N, xd, exact):
     # the many-token one-tile kernel (x ring and weight ring of their own) with
     # partial token tiles and partial channel blocks, on sampled rows
     p = syn.grouped("one-tile", M, K, N, 4, 128, xd, xd, (0.002, 0.02), seed=M + N, int_exact=exact)
-    assert wq.wq_matmul_path(M, K, 4, 128, p.x.dtype, p.scales.dtype) == 2
+    assert wq.wq_matmul_path(M, N, K, 4, 128, p.x.dtype, p.scales.dtype) == 2
     assert wq.wq_workspace_bytes(M, N, K, 4, 128) == 0  # enough tiles: one per CTA, no stream-K
     y = run(p).cpu().numpy().astype(np.float64)
     rng = np.random.default_rng(M)
@@ -160,6 +160,30 @@ def test_prefill_one_tile_ragged(M, K, N, xd, exact):
         assert np.array_equal(y[rows], ref), "max diff %g" % np.max(np.abs(y[rows] - ref))
     else:
         assert_close(y[rows], ref, K, p.name)
+
+
+TWO_TERM = [  # (M, K, N, integer-exact): bf16 below K = 4096 on grids of >= 128 tiles (path 3)
+    (1024, 2048, 4096, False),   # 4 x 32 tiles of 256 tokens x 128 channels
+    (1024, 2048, 4096, True),    # integer-exact: bit for bit
+    (300, 1024, 16400, False),   # 2 x 129 tiles, a 16-channel last block, a partial token tile
+]
+
+
+@pytest.mark.parametrize("M,K,N,exact", TWO_TERM)
+def test_two_term_weights(M, K, N, exact):
+    # each weight enters the MMA as its bf16 rounding plus the bf16 rounding of
+    # the residue: within 2^-16 of the weight, far inside the bound at any K
+    p = syn.grouped("two-term", M, K, N, 4, 128, "bf16", "bf16", (0.002, 0.02), seed=M + N, int_exact=exact)
+    assert wq.wq_matmul_path(M, N, K, 4, 128, p.x.dtype, p.scales.dtype) == 3
+    y = run(p).cpu().numpy().astype(np.float64)
+    rng = np.random.default_rng(M + N)
+    rows = sorted(set([0, 255, 256, M - 1] + rng.choice(np.arange(M), size=12, replace=False).tolist()))
+    ref = oracle_y(p, rows=rows)
+    if exact:
+        assert np.array_equal(y[rows], ref), "max diff %g" % np.max(np.abs(y[rows] - ref))
+    else:
+        err, tol = assert_close(y[rows], ref, K, p.name)
+        assert err <= 0.05 * tol, "two-term weights should sit far inside the bound (%g of it)" % (err / tol)
 
 
 def test_int8_integer_exact_bitwise():
@@ -287,7 +311,7 @@ def test_prefill_persistent_shares_match_one_tile_per_cta(M, K, N, xd):
     # must match the oracle, and each other bit for bit on integer-exact data.
     for exact in (False, True):
         p = syn.grouped("persist", M, K, N, 4, 128, xd, xd, (0.002, 0.02), seed=M + N, int_exact=exact)
-        assert wq.wq_matmul_path(M, K, 4, 128, p.x.dtype, p.scales.dtype) == 2
+        assert wq.wq_matmul_path(M, N, K, 4, 128, p.x.dtype, p.scales.dtype) == 2
         d = to_device(p)
         need = wq.wq_workspace_bytes(M, N, K, 4, 128)
         ws = torch.zeros(need, dtype=torch.uint8, device="cuda")

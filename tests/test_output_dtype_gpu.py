@@ -30,7 +30,7 @@ PATH = {"exact-tc-M100": 1, "prefill-M300": 2}
 def test_16bit_output_is_the_rounded_fp32_result(name, odt):
     p = CASES[name]()
     d = to_device(p)
-    assert wq.wq_matmul_path(p.M, p.K, p.w_bit, p.group_size, p.x.dtype, p.scales.dtype) == PATH.get(name, 0)
+    assert wq.wq_matmul_path(p.M, p.N, p.K, p.w_bit, p.group_size, p.x.dtype, p.scales.dtype) == PATH.get(name, 0)
     y32 = wq.wq_matmul(d["x"], d["packed"], d["scales"], d["zeros"], p.M, p.N, p.K, p.w_bit, p.group_size)
     # a guard band after the 16-bit output must stay untouched
     buf = torch.full((p.M * p.N + 64,), -7.0, dtype=odt, device="cuda")

@@ -50,7 +50,7 @@ def test_noalloc_many_token_problem_runs_one_tile_per_block():
     for exact in (False, True):
         p = syn.grouped("prefill noalloc", 300, 4096, 512, 4, 128, "bf16", "bf16", (0.002, 0.02), seed=9,
                         int_exact=exact)
-        assert wq.wq_matmul_path(p.M, p.K, 4, 128, p.x.dtype, p.scales.dtype) == 2
+        assert wq.wq_matmul_path(p.M, p.N, p.K, 4, 128, p.x.dtype, p.scales.dtype) == 2
         d = to_device(p)
         ref = wq.wq_matmul(d["x"], d["packed"], d["scales"], d["zeros"], p.M, p.N, p.K, 4, 128)
         out = torch.full((p.M, p.N), float("nan"), device="cuda")

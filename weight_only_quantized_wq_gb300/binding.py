@@ -24,7 +24,7 @@ EXPORTS = ("wq_status_string", "wq_chunk_k", "wq_packed_bytes", "wq_pack", "wq_u
            "wq_workspace_bytes", "wq_matmul", "wq_matmul_ex", "wq_matmul_noalloc", "wq_matmul_path",
            "wq_t2_pack", "wq_t2_workspace_bytes", "wq_t2_matmul", "wq_check_device")
 
-PATHS = {0: "decode_kernel", 1: "midm_kernel", 2: "prefill_kernel"}
+PATHS = {0: "decode_kernel", 1: "midm_kernel", 2: "prefill_kernel", 3: "prefill_kernel"}
 
 # the failure-path test hook of include/wq_testing.h
 TESTING_EXPORTS = ("wq_testing_decode_timeout",)
@@ -73,7 +73,7 @@ def lib() -> ctypes.CDLL:
         L.wq_t2_matmul.restype = I
         L.wq_t2_matmul.argtypes = [P, P, I, I, I, P, P, Z, P]
         L.wq_matmul_path.restype = I
-        L.wq_matmul_path.argtypes = [I, I, I, I, I, I]
+        L.wq_matmul_path.argtypes = [I, I, I, I, I, I, I]
         L.wq_testing_decode_timeout.restype = I
         L.wq_testing_decode_timeout.argtypes = [P, I, P, P, I, P, I, I, I, I, I, P, P, Z, ctypes.c_longlong, I, P]
         L.wq_check_device.restype = I
@@ -235,12 +235,12 @@ def wq_t2_matmul(x: torch.Tensor, packed_w: torch.Tensor, M: int, N: int, K: int
     return out
 
 
-def wq_matmul_path(M: int, K: int, w_bit: int, group_size: int, x_dtype, s_dtype) -> int:
-    """Kernel family wq_matmul runs (0 few-token, 1 exact tensor-core, 2 many-token; -1 invalid).
-    Dtypes are torch dtypes or the WQ_* codes."""
+def wq_matmul_path(M: int, N: int, K: int, w_bit: int, group_size: int, x_dtype, s_dtype) -> int:
+    """Kernel family wq_matmul runs (0 few-token, 1 exact tensor-core, 2 many-token, 3 many-token
+    with two-term weights; -1 invalid).  Dtypes are torch dtypes or the WQ_* codes."""
     xd = _DTYPE.get(x_dtype, x_dtype)
     sd = _DTYPE.get(s_dtype, s_dtype)
-    return lib().wq_matmul_path(M, K, w_bit, group_size, int(xd), int(sd))
+    return lib().wq_matmul_path(M, N, K, w_bit, group_size, int(xd), int(sd))
 
 
 def wq_testing_decode_timeout(x: torch.Tensor, packed_w: torch.Tensor, scales: torch.Tensor,

@@ -137,14 +137,20 @@ wq_status prepare_call(const void *x, wq_dtype x_dtype, const void *packed_w, co
 
 Route route_of(const MatmulArgs &a) {
   if (a.w_bit != 4 || !midm_supported(a) || a.M <= kDecodeMaxM) return Route::kDecode;
-  if (a.M >= kPrefillMinM && prefill_supported(a) && prefill_within_tolerance(a)) return Route::kPrefill;
+  if (a.M >= kPrefillMinM && prefill_supported(a)) {
+    if (prefill_within_tolerance(a)) return Route::kPrefill;
+    const long long tiles = (long long)((a.M + 255) / 256) * ((a.N + 127) / 128);  // of the two-term kernel
+    if (a.M >= kSplitMinM && tiles >= kSplitMinTiles) return Route::kPrefillSplit;
+  }
   return Route::kMidm;
 }
 
 wq_status run_call(const Call &c, void *workspace, size_t workspace_bytes, void *stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (c.route == Route::kPrefill)
-    return launch_prefill(c.a, c.sms, workspace, workspace_bytes, s) == cudaSuccess ? WQ_OK : WQ_ERR_CUDA;
+  if (c.route == Route::kPrefill || c.route == Route::kPrefillSplit)
+    return launch_prefill(c.a, c.sms, workspace, workspace_bytes, c.route == Route::kPrefillSplit, s) == cudaSuccess
+               ? WQ_OK
+               : WQ_ERR_CUDA;
   if (c.route == Route::kMidm) {
     const MidmPlan pl = plan_midm(c.a.M, c.a.N, c.a.K, c.sms);
     return launch_midm(c.a, pl, s) == cudaSuccess ? WQ_OK : WQ_ERR_CUDA;
@@ -349,11 +355,12 @@ wq_status wq_t2_matmul(const int8_t *x, const void *packed_w, int M, int N, int 
   return wq::run_call(c, workspace, xoff, stream);
 }
 
-int wq_matmul_path(int M, int K, int w_bit, int group_size, wq_dtype x_dtype, wq_dtype s_dtype) {
-  if (!valid_wbit(w_bit) || M < 0 || K <= 0 || K % (256 / w_bit) != 0) return -1;
+int wq_matmul_path(int M, int N, int K, int w_bit, int group_size, wq_dtype x_dtype, wq_dtype s_dtype) {
+  if (!valid_wbit(w_bit) || M < 0 || N <= 0 || N % 16 != 0 || K <= 0 || K % (256 / w_bit) != 0) return -1;
   if (x_dtype != WQ_F16 && x_dtype != WQ_BF16) return -1;
   wq::MatmulArgs a{};
   a.M = M;
+  a.N = N;
   a.K = K;
   a.w_bit = w_bit;
   a.x_bf16 = x_dtype == WQ_BF16;
@@ -370,6 +377,7 @@ int wq_matmul_path(int M, int K, int w_bit, int group_size, wq_dtype x_dtype, wq
     case wq::Route::kDecode: return 0;
     case wq::Route::kMidm: return 1;
     case wq::Route::kPrefill: return 2;
+    case wq::Route::kPrefillSplit: return 3;
   }
   return -1;
 }

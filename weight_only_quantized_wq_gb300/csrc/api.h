@@ -14,6 +14,7 @@ enum class Route {
   kDecode,   // few tokens, or codes / groups the tensor-core paths do not take (64-token slices)
   kMidm,     // tensor cores, exact weights, group scale in fp32
   kPrefill,  // tensor cores, weight rounded once to the x dtype (many tokens)
+  kPrefillSplit,  // the same kernel, each weight as two terms (rounded, residue): bf16 below K = 4096
 };
 
 // Route of a validated call (x and scale dtypes only matter for kPrefill).

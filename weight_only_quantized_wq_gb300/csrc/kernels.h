@@ -80,7 +80,11 @@ bool prefill_supported(const MatmulArgs &a);
 // tile per CTA.
 // The flags share the workspace's zero-filled counter region.
 size_t prefill_workspace_bytes(int M, int N, int K, int sms);
-cudaError_t launch_prefill(const MatmulArgs &a, int sms, void *workspace, size_t workspace_bytes, cudaStream_t s);
+// split_w: each weight as two terms in the x dtype (w rounded, and the
+// rounding residue rounded; within 2^-16 of w), 128 channels per tile, one
+// tile per CTA.  For calls where one rounding would exceed the accepted error.
+cudaError_t launch_prefill(const MatmulArgs &a, int sms, void *workspace, size_t workspace_bytes, bool split_w,
+                           cudaStream_t s);
 
 // Tensor-core path for a moderate number of tokens (int4 codes, group size
 // a multiple of 64): exact weights, group scales applied in fp32.
@@ -104,6 +108,17 @@ constexpr int kDecodeMaxM = 64;
 // dtype) takes over; calls it cannot take within the accepted error, or with
 // a scale dtype other than the x dtype, run on the exact tensor-core kernel.
 constexpr int kPrefillMinM = 65;
+// Where one rounding of the weight would exceed the accepted error (bf16
+// below K = 4096), the many-token kernel with each weight as two terms
+// (rounded weight and rounded residue, 128 channels per tile) against the
+// exact tensor-core kernel, measured with bf16 int4 g128: on the K = 2048,
+// N = 28672 weights 57 / 86 / 170 us against 69 / 136 / 270 us at M = 256 /
+// 512 / 1024 and equal at 128; with fewer tiles it loses (M = 256, N = 4096:
+// 32 tiles, 28 against 17 us; M = 128, N = 8192: 64 tiles, 25 against 17 us)
+// and wins from 128 tiles (M = 1024 or 2048 on N = 4096 or 2048: 29 against
+// 46 us; M = 256, K = 1024, N = 16384: 19 against 28 us).
+constexpr int kSplitMinM = 129;
+constexpr int kSplitMinTiles = 128;  // ceil(M / 256) x ceil(N / 128)
 // The many-token kernel rounds each dequantized weight once to the x dtype
 // (relative error up to 2^-11 for fp16, 2^-9 for bf16).  Over random signs
 // the result's error stays near that bound / sqrt(3) of the output's RMS, a

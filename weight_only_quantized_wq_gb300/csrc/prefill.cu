@@ -157,6 +157,16 @@ __device__ __forceinline__ uint32_t mul2(uint32_t a, uint32_t b) {
   return d;
 }
 
+template <bool BF16>
+__device__ __forceinline__ uint32_t fma2(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  if constexpr (BF16)
+    asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  else
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
 // 32 consecutive fp32 columns of this warp's TMEM lane quarter.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   uint32_t r[32];
@@ -468,9 +478,17 @@ __global__ void __launch_bounds__(SK_THREADS, 1) prefill_sk_kernel(const __grid_
 
 // One tile per CTA (blockIdx.x: token tile, blockIdx.y: channel block); warps
 // 4..7 read the accumulator out after their share of the dequant.
-template <bool BF16, bool ZERO, int MS>
+// SPLIT: each weight enters the MMA as two terms, w1 = w rounded to the x
+// dtype and w2 = (w - w1) rounded (w2 from one fma: (q - z) s - w1 exactly,
+// then one rounding), so w1 + w2 is w within 2^-16 of it instead of 2^-8;
+// the tile is then 128 channels, w1 in the B rows 0..127 and w2 in 128..255
+// of the same 256-row operand, and the epilogue adds the two halves of the
+// accumulator.  Twice the MMA work per weight, for calls where one rounding
+// would exceed the accepted error (bf16 below K = 4096).
+template <bool BF16, bool ZERO, int MS, bool SPLIT>
 __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_constant__ Params p) {
   using C = DCfg<MS>;
+  constexpr int CB = SPLIT ? BN / 2 : BN;  // output channels per tile
   constexpr int MSUB = C::MSUB, BM = C::BM, A_BYTES = C::A_BYTES, XS = C::XS, WS = C::WS;
   constexpr int W_SLOT = C::W_SLOT, TMEM_COLS = C::TMEM_COLS;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -493,9 +511,9 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
   // Token tiles vary fastest across the grid, so the CTAs that read the same
   // 256-channel weight block run at about the same time and share it in L2.
   const int mb = blockIdx.x, nb = blockIdx.y;
-  const int n0 = nb * BN, m0 = mb * BM;
+  const int n0 = nb * CB, m0 = mb * BM;
   const int nt0 = n0 / 16;
-  const int ntiles = min(BN / 16, p.nt_total - nt0);
+  const int ntiles = min(CB / 16, p.nt_total - nt0);
   const int nk = p.K / BK;
 
   if (threadIdx.x == 0) {
@@ -550,7 +568,7 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
         const uint32_t fb = smem_addr(&wfull[s]);
         const uint32_t base = smem_addr(wring + s * W_SLOT);
         const int g = i * BK / p.gs;
-        mbar_arrive_expect_tx(fb, ntiles * 512 + S_BYTES + (ZERO ? Z_BYTES : 0));
+        mbar_arrive_expect_tx(fb, ntiles * 512 + CB * 2 + (ZERO ? CB * 4 : 0));  // scale and zero boxes of CB
         bulk_g2s(base, p.packed + ((size_t)i * p.nt_total + nt0) * 512, ntiles * 512, fb, pol);
         tma_load_2d(base + W_BYTES, &p.tm_s, n0, g, fb);
         if (ZERO) tma_load_2d(base + W_BYTES + S_BYTES, &p.tm_z, n0, g / 8, fb);
@@ -592,10 +610,11 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
       const int g = i * BK / p.gs;
       // This thread's words, scales and zeros of the stage into registers;
       // then the weight slot goes back to the producer.
+      constexpr int HALVES = CB * 2 / 256;  // (tile, lane) pairs per thread
       uint4 wv[2];
       uint32_t zz[2][2], ss[2][2];
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
+      for (int half = 0; half < HALVES; ++half) {
         const int pr = dq + half * 256;  // (tile, lane) pair 0..511
         const int tile = pr >> 5, ln = tc::dq_slot(pr & 31);
         wv[half] = make_uint4(0u, 0u, 0u, 0u);
@@ -617,7 +636,7 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
       if (i >= BSTAGES && !mbar_wait(smem_addr(&bempty[sb]), ((i / BSTAGES) - 1) & 1, p.err, abort_flag)) break;
       const uint32_t bdst = smem_addr(bbuf + sb * B_BYTES);
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
+      for (int half = 0; half < HALVES; ++half) {
         const int pr = dq + half * 256;
         const int tile = pr >> 5, ln = tc::dq_slot(pr & 31);
         if (tile < ntiles) {
@@ -631,11 +650,17 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
               const uint32_t w = w4[2 * u + r];
 #pragma unroll
               for (int j = 0; j < 2; ++j) {
-                const uint32_t lo = mul2<BF16>(sub_pair<BF16>(code_pair<4, BF16>(w, 2 * j), zz[half][r]), ss[half][r]);
-                const uint32_t hi =
-                    mul2<BF16>(sub_pair<BF16>(code_pair<4, BF16>(w, 2 * j + 1), zz[half][r]), ss[half][r]);
+                const uint32_t d0 = sub_pair<BF16>(code_pair<4, BF16>(w, 2 * j), zz[half][r]);      // q - z, exact
+                const uint32_t d1 = sub_pair<BF16>(code_pair<4, BF16>(w, 2 * j + 1), zz[half][r]);
+                const uint32_t lo = mul2<BF16>(d0, ss[half][r]);
+                const uint32_t hi = mul2<BF16>(d1, ss[half][r]);
                 const int k = 32 * u + 16 * j + 4 * tq;
                 sts64(bdst + tc::sw128_off(col, k), lo, hi);
+                if constexpr (SPLIT) {  // the rounding residues, in B rows 128..255
+                  const uint32_t lo2 = fma2<BF16>(d0, ss[half][r], lo ^ 0x80008000u);
+                  const uint32_t hi2 = fma2<BF16>(d1, ss[half][r], hi ^ 0x80008000u);
+                  sts64(bdst + tc::sw128_off(col + BN / 2, k), lo2, hi2);
+                }
               }
             }
           }
@@ -652,9 +677,15 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
       tc::fence_after();
       for (int h = 0; h < MSUB; ++h) {
         const int m = m0 + h * UM + q * 32 + lane;
-        for (int c = 0; c < BN; c += 32) {
+        for (int c = 0; c < CB; c += 32) {
           float v[32];
           tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + h * BN + c, v);
+          if constexpr (SPLIT) {  // + the residue terms' columns
+            float v2[32];
+            tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + h * BN + BN / 2 + c, v2);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] += v2[j];
+          }
           if (m < p.M) {
             const size_t row = (size_t)m * p.N + n0 + c;
             if (n0 + c + 32 <= p.N) {
@@ -686,9 +717,9 @@ bool prefill_supported(const MatmulArgs &a) {
   return a.w_bit == 4 && a.group_size % pf::BK == 0 && a.K % pf::BK == 0 && a.x_bf16 == a.s_bf16;
 }
 
-template <bool BF16, bool ZERO, int MS>
+template <bool BF16, bool ZERO, int MS, bool SPLIT>
 static cudaError_t launch_t(const pf::Params &pp, dim3 grid, bool persistent, cudaStream_t s) {
-  auto kern = persistent ? pf::prefill_sk_kernel<BF16, ZERO, MS> : pf::prefill_kernel<BF16, ZERO, MS>;
+  auto kern = persistent ? pf::prefill_sk_kernel<BF16, ZERO, MS> : pf::prefill_kernel<BF16, ZERO, MS, SPLIT>;
   static int attr_set[64][2] = {{0}};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
@@ -715,10 +746,17 @@ static cudaError_t launch_t(const pf::Params &pp, dim3 grid, bool persistent, cu
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
+template <int MS, bool SPLIT>
+static cudaError_t launch_ms_s(const pf::Params &pp, dim3 grid, bool sk, bool bf16, bool z, cudaStream_t s) {
+  if (bf16)
+    return z ? launch_t<true, true, MS, SPLIT>(pp, grid, sk, s) : launch_t<true, false, MS, SPLIT>(pp, grid, sk, s);
+  return z ? launch_t<false, true, MS, SPLIT>(pp, grid, sk, s) : launch_t<false, false, MS, SPLIT>(pp, grid, sk, s);
+}
+
 template <int MS>
-static cudaError_t launch_ms(const pf::Params &pp, dim3 grid, bool sk, bool bf16, bool z, cudaStream_t s) {
-  if (bf16) return z ? launch_t<true, true, MS>(pp, grid, sk, s) : launch_t<true, false, MS>(pp, grid, sk, s);
-  return z ? launch_t<false, true, MS>(pp, grid, sk, s) : launch_t<false, false, MS>(pp, grid, sk, s);
+static cudaError_t launch_ms(const pf::Params &pp, dim3 grid, bool sk, bool bf16, bool z, bool split,
+                             cudaStream_t s) {
+  return split ? launch_ms_s<MS, true>(pp, grid, false, bf16, z, s) : launch_ms_s<MS, false>(pp, grid, sk, bf16, z, s);
 }
 
 // CTAs of the persistent launch: one per SM (the kernel's shared memory and
@@ -737,18 +775,20 @@ size_t prefill_workspace_bytes(int M, int N, int K, int sms) {
   return (size_t)pf::kFlagBytes + (size_t)prefill_ctas(tiles, units, sms) * bm * pf::BN * sizeof(float);
 }
 
-cudaError_t launch_prefill(const MatmulArgs &a, int sms, void *workspace, size_t workspace_bytes, cudaStream_t s) {
+cudaError_t launch_prefill(const MatmulArgs &a, int sms, void *workspace, size_t workspace_bytes, bool split_w,
+                           cudaStream_t s) {
   pf::Params pp{};
   const int G = a.K / a.group_size;
   // One 128-token accumulator per tile up to 128 tokens, two (256 tokens) beyond.
   const int ms = a.M <= pf::UM ? 1 : 2;
   const int bm = pf::UM * ms;
+  const int cb = split_w ? pf::BN / 2 : pf::BN;  // output channels per tile
   if (!encode_2d(&pp.tm_x, a.x, 2, (uint64_t)a.K, (uint64_t)a.M, pf::BK, (uint32_t)bm, 128))
     return cudaErrorInvalidValue;
-  if (!encode_2d(&pp.tm_s, a.scales, 2, (uint64_t)a.N, (uint64_t)G, pf::BN, 1, 0))
+  if (!encode_2d(&pp.tm_s, a.scales, 2, (uint64_t)a.N, (uint64_t)G, (uint32_t)cb, 1, 0))
     return cudaErrorInvalidValue;
   if (a.zeros &&
-      !encode_2d(&pp.tm_z, a.zeros, 4, (uint64_t)a.N, (uint64_t)((G + 7) / 8), pf::BN, 1, 0))
+      !encode_2d(&pp.tm_z, a.zeros, 4, (uint64_t)a.N, (uint64_t)((G + 7) / 8), (uint32_t)cb, 1, 0))
     return cudaErrorInvalidValue;
   pp.packed = static_cast<const uint8_t *>(a.packed);
   pp.out = a.out;
@@ -768,9 +808,9 @@ cudaError_t launch_prefill(const MatmulArgs &a, int sms, void *workspace, size_t
   // with stream-K shares.  With at least half the SMs busy, one tile per CTA
   // measured faster on the 8192 x 28672 weights (no fix-ups, and neighbouring
   // CTAs share each weight block in L2).
-  dim3 grid((unsigned)pp.tiles_m, (unsigned)((a.N + pf::BN - 1) / pf::BN));
+  dim3 grid((unsigned)pp.tiles_m, (unsigned)((a.N + cb - 1) / cb));
   bool sk = false;
-  const size_t want = prefill_workspace_bytes(a.M, a.N, a.K, sms);
+  const size_t want = split_w ? 0 : prefill_workspace_bytes(a.M, a.N, a.K, sms);
   if (want > 0 && workspace && workspace_bytes >= want) {
     grid = dim3((unsigned)prefill_ctas(tiles, pp.units, sms));
     sk = true;
@@ -778,7 +818,8 @@ cudaError_t launch_prefill(const MatmulArgs &a, int sms, void *workspace, size_t
     pp.partial = reinterpret_cast<float *>(static_cast<char *>(workspace) + pf::kFlagBytes);
   }
   const bool z = a.zeros != nullptr;
-  return ms == 1 ? launch_ms<1>(pp, grid, sk, a.x_bf16, z, s) : launch_ms<2>(pp, grid, sk, a.x_bf16, z, s);
+  return ms == 1 ? launch_ms<1>(pp, grid, sk, a.x_bf16, z, split_w, s)
+                 : launch_ms<2>(pp, grid, sk, a.x_bf16, z, split_w, s);
 }
 
 }  // namespace wq
