@@ -21,8 +21,9 @@ CASES = {  # name -> problem; the comment gives the kernel path
     "decode-64-row-slices": lambda: syn.grouped("sl", 100, 1024, 272, 4, 32, "f16", "f16", (0.002, 0.02), seed=24),
     "exact-tc-M100": lambda: syn.grouped("tc", 100, 2048, 400, 4, 128, "bf16", "bf16", (0.002, 0.02), seed=25),
     "prefill-M300": lambda: syn.grouped("pf", 300, 4096, 272, 4, 128, "bf16", "bf16", (0.002, 0.02), seed=26),
+    "two-term-M129": lambda: syn.grouped("tt", 129, 512, 16384, 4, 128, "bf16", "bf16", (0.002, 0.02), seed=27),
 }
-PATH = {"exact-tc-M100": 1, "prefill-M300": 2}
+PATH = {"exact-tc-M100": 1, "prefill-M300": 2, "two-term-M129": 3}
 
 
 @pytest.mark.parametrize("name", sorted(CASES))
