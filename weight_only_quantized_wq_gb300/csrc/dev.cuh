@@ -149,27 +149,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, int 
 }
 
 
-// Prefetch `bytes` (multiple of 16, 16-byte aligned) of global memory into L2.
-__device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
-
-// Prefetch one box of a 2-D tensor map into L2.
-__device__ __forceinline__ void prefetch_tma_2d(const void *tmap, int c0, int c1) {
-  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global [%0, {%1, %2}];" ::"l"(tmap), "r"(c0), "r"(c1)
-               : "memory");
-}
-
-// ---------------------------------------------------------------- grid dependencies
-// Programmatic dependent launch.  Without the launch attribute both are no-ops.
-// Let the next grid on the stream be scheduled (its CTAs block in their wait).
-__device__ __forceinline__ void grid_launch_dependents() {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-// Block until every prerequisite grid has completed and its memory
-// operations are visible to this grid.
-__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-
 // ---------------------------------------------------------------- clusters
 // Barrier over every thread of every CTA of the cluster (release / acquire).
 __device__ __forceinline__ void cluster_sync() {
