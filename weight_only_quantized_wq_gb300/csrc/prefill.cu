@@ -45,8 +45,10 @@
 // of which 4..7 read the accumulator out at the end.
 // The scale and zero are applied to the weight (one rounding to bf16/fp16),
 // since a per-group rescale of a 128 x 256 TMEM accumulator would cost more
-// than the tensor cores gain; calls where that rounding could exceed the
-// accepted error run on the exact tensor-core kernel instead.
+// than the tensor cores gain.  Calls where that rounding could exceed the
+// accepted error run the one-tile kernel with two-term weights (the rounded
+// weight and its rounded residue, 128 channels per tile) when they have
+// enough tiles, else the exact tensor-core kernel.
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
