@@ -81,7 +81,9 @@ static DecodePlan plan_decode_search(int M, int N, int K, int w_bit, int group_s
                                      bool unit_scale) {
   DecodePlan best{};
   const int rows = M < 64 ? M : 64;
-  const int mt = rows <= 8 ? 1 : rows <= 16 ? 2 : rows <= 32 ? 4 : 8;
+  // token octets per MMA column block: the MMAs per weight fragment grow with
+  // it, so it follows M closely (every octet is one more mma.sync per fragment)
+  const int mt = rows <= 8 ? 1 : rows <= 16 ? 2 : rows <= 24 ? 3 : rows <= 32 ? 4 : rows <= 48 ? 6 : 8;
   const int kc = 256 / w_bit;
   const int nt = N / 16;
   const int kch = K / kc;
@@ -89,8 +91,8 @@ static DecodePlan plan_decode_search(int M, int N, int K, int w_bit, int group_s
   const bool grouped = w_bit != 8;
   const int V = 32 / w_bit;
   // Two 16-channel tiles per warp (the CTA covers 128 channels) keep three
-  // CTAs of four consumer warps on an SM; 64-row slices take one.
-  const int tn = mt == 8 ? 1 : 2;
+  // CTAs of four consumer warps on an SM; 48- and 64-row slices take one.
+  const int tn = mt >= 6 ? 1 : 2;
   const int nblocks = (nt + kDecodeWarps * tn - 1) / (kDecodeWarps * tn);
   const double unit_bytes = (double)tn * kDecodeWarps * 512.0;  // one chunk row of a CTA
   const int fold = fold_for(w_bit, gs);
