@@ -92,7 +92,7 @@ static DecodePlan plan_decode_search(int M, int N, int K, int w_bit, int group_s
   const int V = 32 / w_bit;
   // Two 16-channel tiles per warp (the CTA covers 128 channels) keep three
   // CTAs of four consumer warps on an SM; 48- and 64-row slices take one.
-  const int tn = mt >= 6 ? 1 : 2;
+  const int tn = mt >= 4 ? 1 : 2;
   const int nblocks = (nt + kDecodeWarps * tn - 1) / (kDecodeWarps * tn);
   const double unit_bytes = (double)tn * kDecodeWarps * 512.0;  // one chunk row of a CTA
   const int fold = fold_for(w_bit, gs);

@@ -59,13 +59,16 @@ namespace wq {
 constexpr int kDecodeWarps = 4;  // consumer warps per CTA (plus one producer warp)
 constexpr int kDecodeThreads = (kDecodeWarps + 1) * 32;
 constexpr int kDecodeHeader = 256;  // mbarriers in front of the staged rows
-// Ring depth in chunk rows (slots): 12 to 24 KB of weights in flight per CTA.
-__host__ __device__ constexpr int decode_stages(int) { return 6; }
+// Ring depth in chunk rows (slots): 12 to 24 KB of weights in flight per CTA;
+// 8-octet token tiles (64 rows of x per slot) keep 4, so that three CTAs fit
+// an SM's shared memory (measured 86.6 against 96.5 us at c5 M=64).
+__host__ __device__ constexpr int decode_stages(int mt) { return mt >= 8 ? 4 : 6; }
 // A ring stage holds this many chunk rows (slots): one barrier wait and one
 // release per pair of chunk rows.
 constexpr int kSlotsPerStage = 2;
 // Resident CTAs per SM the register budget is sized for.
-__host__ __device__ constexpr int decode_min_blocks(int mt, int tn) { return mt * tn >= 8 ? 2 : 3; }
+// (every shape compiles to at most ~122 registers under this bound, no spills)
+__host__ __device__ constexpr int decode_min_blocks(int, int) { return 3; }
 
 __host__ __device__ constexpr int align128(int v) { return (v + 127) / 128 * 128; }
 
@@ -92,7 +95,7 @@ struct DecodeSmem {
   __host__ __device__ constexpr int x_bytes() const { return mt * 8 * x_pitch(w); }
   __host__ __device__ constexpr int slot_bytes() const { return align128(x_off() + x_bytes()); }
   __host__ __device__ constexpr int stage_bytes() const { return kSlotsPerStage * slot_bytes(); }
-  __host__ __device__ constexpr int bytes() const { return ring_off() + decode_stages(tn) * slot_bytes(); }
+  __host__ __device__ constexpr int bytes() const { return ring_off() + decode_stages(mt) * slot_bytes(); }
 };
 
 struct DecodeParams {
@@ -125,7 +128,7 @@ template <int W, bool BF16, int MT, int TN, bool ZERO, int FOLD>
 __global__ void __launch_bounds__(kDecodeThreads, decode_min_blocks(MT, TN))
     decode_kernel(const __grid_constant__ DecodeParams p) {
   using G = Geo<W>;
-  constexpr int NW = kDecodeWarps, STAGES = decode_stages(TN) / kSlotsPerStage;
+  constexpr int NW = kDecodeWarps, STAGES = decode_stages(MT) / kSlotsPerStage;
   constexpr int SLOT = DecodeSmem{W, MT, TN, 0, 0, 0}.slot_bytes();
   constexpr int KS = G::KS, KC = G::KC, WK = G::WK, V = G::V;
   constexpr int XP = x_pitch(W);

@@ -16,7 +16,7 @@ cudaError_t launch_decode_wf<WQ_W, WQ_FOLD>(const DecodeParams &dp, const Decode
   WQ_DECODE_CASE(WQ_W, BF, 1, 2, Z, WQ_FOLD) \
   WQ_DECODE_CASE(WQ_W, BF, 2, 2, Z, WQ_FOLD) \
   WQ_DECODE_CASE(WQ_W, BF, 3, 2, Z, WQ_FOLD) \
-  WQ_DECODE_CASE(WQ_W, BF, 4, 2, Z, WQ_FOLD) \
+  WQ_DECODE_CASE(WQ_W, BF, 4, 1, Z, WQ_FOLD) \
   WQ_DECODE_CASE(WQ_W, BF, 6, 1, Z, WQ_FOLD) \
   WQ_DECODE_CASE(WQ_W, BF, 8, 1, Z, WQ_FOLD)
 #if WQ_W == 8
@@ -38,7 +38,7 @@ long decode_capacity_wf<WQ_W, WQ_FOLD>(int mt, int tn, bool zero, int smem, int 
   WQ_DECODE_CAPACITY(WQ_W, 1, 2, Z, WQ_FOLD) \
   WQ_DECODE_CAPACITY(WQ_W, 2, 2, Z, WQ_FOLD) \
   WQ_DECODE_CAPACITY(WQ_W, 3, 2, Z, WQ_FOLD) \
-  WQ_DECODE_CAPACITY(WQ_W, 4, 2, Z, WQ_FOLD) \
+  WQ_DECODE_CAPACITY(WQ_W, 4, 1, Z, WQ_FOLD) \
   WQ_DECODE_CAPACITY(WQ_W, 6, 1, Z, WQ_FOLD) \
   WQ_DECODE_CAPACITY(WQ_W, 8, 1, Z, WQ_FOLD)
 #if WQ_W == 8
