@@ -54,7 +54,7 @@ def test_prefill_sweep_sampled_rows(M):
     assert np.all(np.isfinite(y))
 
 
-@pytest.mark.parametrize("M", [24, 32, 48, 96, 128, 192])
+@pytest.mark.parametrize("M", [20, 24, 32, 40, 48, 56, 96, 128, 192])
 def test_sweep_weights_mid_m_sampled_rows(M):
     # the large weights at token counts between the workloads' ones: the
     # few-token kernel with 32- and 64-row token tiles (several waves of
@@ -112,6 +112,8 @@ INT_EXACT = [  # (name, M, K, N, w_bit, group, x, s, symmetric)
     ("int2-g32-f16", 2, 1024, 128, 2, 32, "f16", "bf16", False),
     ("int4-asym-bf16-M24-N400", 24, 2048, 400, 4, 64, "bf16", "bf16", False),
     ("int4-perchannel-bf16-M40", 40, 1024, 256, 4, 1024, "bf16", "bf16", False),
+    ("int4-asym-f16-M52-N176", 52, 2048, 176, 4, 128, "f16", "f16", False),   # 7-octet token tile
+    ("int2-asym-bf16-M21", 21, 4096, 96, 2, 64, "bf16", "bf16", False),      # 3-octet token tile
     # more tokens: the exact tensor-core path (tcgen05, group scale in fp32) ...
     ("int4-asym-bf16-M200", 200, 1024, 512, 4, 128, "bf16", "bf16", False),
     ("int4-asym-f16x-bf16s-M70", 70, 1024, 128, 4, 256, "f16", "bf16", False),

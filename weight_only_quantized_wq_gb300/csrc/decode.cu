@@ -83,7 +83,7 @@ static DecodePlan plan_decode_search(int M, int N, int K, int w_bit, int group_s
   const int rows = M < 64 ? M : 64;
   // token octets per MMA column block: the MMAs per weight fragment grow with
   // it, so it follows M closely (every octet is one more mma.sync per fragment)
-  const int mt = rows <= 8 ? 1 : rows <= 16 ? 2 : rows <= 24 ? 3 : rows <= 32 ? 4 : rows <= 48 ? 6 : 8;
+  const int mt = rows <= 32 ? (rows + 7) / 8 : rows <= 40 ? 5 : rows <= 48 ? 6 : rows <= 56 ? 7 : 8;
   const int kc = 256 / w_bit;
   const int nt = N / 16;
   const int kch = K / kc;

@@ -60,9 +60,10 @@ constexpr int kDecodeWarps = 4;  // consumer warps per CTA (plus one producer wa
 constexpr int kDecodeThreads = (kDecodeWarps + 1) * 32;
 constexpr int kDecodeHeader = 256;  // mbarriers in front of the staged rows
 // Ring depth in chunk rows (slots): 12 to 24 KB of weights in flight per CTA;
-// 8-octet token tiles (64 rows of x per slot) keep 4, so that three CTAs fit
-// an SM's shared memory (measured 86.6 against 96.5 us at c5 M=64).
-__host__ __device__ constexpr int decode_stages(int mt) { return mt >= 8 ? 4 : 6; }
+// 7- and 8-octet token tiles (56 or 64 rows of x per slot) keep 4, so that
+// three CTAs fit an SM's shared memory (measured 86.6 against 96.5 us at c5
+// M=64 with 8 octets).
+__host__ __device__ constexpr int decode_stages(int mt) { return mt >= 7 ? 4 : 6; }
 // A ring stage holds this many chunk rows (slots): one barrier wait and one
 // release per pair of chunk rows.
 constexpr int kSlotsPerStage = 2;

@@ -17,7 +17,9 @@ cudaError_t launch_decode_wf<WQ_W, WQ_FOLD>(const DecodeParams &dp, const Decode
   WQ_DECODE_CASE(WQ_W, BF, 2, 2, Z, WQ_FOLD) \
   WQ_DECODE_CASE(WQ_W, BF, 3, 2, Z, WQ_FOLD) \
   WQ_DECODE_CASE(WQ_W, BF, 4, 1, Z, WQ_FOLD) \
+  WQ_DECODE_CASE(WQ_W, BF, 5, 1, Z, WQ_FOLD) \
   WQ_DECODE_CASE(WQ_W, BF, 6, 1, Z, WQ_FOLD) \
+  WQ_DECODE_CASE(WQ_W, BF, 7, 1, Z, WQ_FOLD) \
   WQ_DECODE_CASE(WQ_W, BF, 8, 1, Z, WQ_FOLD)
 #if WQ_W == 8
   SHAPES(true, false)
@@ -39,7 +41,9 @@ long decode_capacity_wf<WQ_W, WQ_FOLD>(int mt, int tn, bool zero, int smem, int 
   WQ_DECODE_CAPACITY(WQ_W, 2, 2, Z, WQ_FOLD) \
   WQ_DECODE_CAPACITY(WQ_W, 3, 2, Z, WQ_FOLD) \
   WQ_DECODE_CAPACITY(WQ_W, 4, 1, Z, WQ_FOLD) \
+  WQ_DECODE_CAPACITY(WQ_W, 5, 1, Z, WQ_FOLD) \
   WQ_DECODE_CAPACITY(WQ_W, 6, 1, Z, WQ_FOLD) \
+  WQ_DECODE_CAPACITY(WQ_W, 7, 1, Z, WQ_FOLD) \
   WQ_DECODE_CAPACITY(WQ_W, 8, 1, Z, WQ_FOLD)
 #if WQ_W == 8
   SHAPES(false)
